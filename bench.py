@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the hot path: one step = fused RoPE-and-append + paged GQA attention over a
+seeded synthetic batch shaped like a Qwen3-0.6B decode layer at 256 concurrent sequences
+(16 q / 8 kv heads, head_dim 128, contexts uniform in [100, 2048], a quarter of the
+sequences sharing up to 32 prefix blocks, 40000-block pool).
+
+Prints ONE JSON line (rank 0).  ``value`` is the unique KV bytes the step must read divided
+by the device time of the whole step (kv_append + paged_attention), in GB/s.  The roofline
+object is for the dominant kernel (decode split-K), timed live with CUDA events recorded by
+the library around that kernel on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--workload I]
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this path has) on the
+host cores, on a bounded sample of the same workload.  With N > 1 (torchrun) every rank runs
+an independent replica (the path has no exchange step); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_gqa_14_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention achieved KV GB/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------------ workload facts
+def kv_unique_bytes(bt):
+    """K+V bytes of every distinct (physical slot, kv head) the step's attention reads."""
+    rows = set()
+    for b in range(bt.num_seqs):
+        n = int(bt.query_start_loc[b + 1] - bt.query_start_loc[b])
+        if n == 0:
+            continue
+        ctx = int(bt.context_lens[b])
+        for j in range(-(-ctx // 16)):
+            blk = int(bt.block_tables[b, j])
+            last = min(16, ctx - 16 * j)
+            rows.update((blk, r) for r in range(last))
+    return len(rows) * bt.num_kv_heads * bt.head_dim * 2 * 2
+
+
+def kv_logical_bytes(bt):
+    spans = np.diff(bt.query_start_loc)
+    return int(bt.context_lens[spans > 0].astype(np.int64).sum()) * bt.num_kv_heads * bt.head_dim * 2 * 2
+
+
+def decode_algorithmic_bytes(bt, kv_unique):
+    """Algorithmic bytes of one decode-kernel launch: unique KV + q read + out write + tables."""
+    qo = 2 * bt.num_tokens * bt.num_q_heads * bt.head_dim * 2
+    tables = int((-(-bt.context_lens.astype(np.int64) // 16)).sum()) * 4 + bt.num_seqs * 8
+    return kv_unique + qo + tables
+
+
+def sub_batch(bt, seqs):
+    """A batch of the chosen sequences with a compact pool (for host-side oracle timing)."""
+    seqs = list(seqs)
+    blocks = sorted({int(x) for b in seqs for x in bt.block_tables[b] if x >= 0})
+    remap = {b: i for i, b in enumerate(blocks)}
+    idx = np.array(blocks, dtype=np.int64)
+    rows = []
+    qsl = [0]
+    for b in seqs:
+        s, e = int(bt.query_start_loc[b]), int(bt.query_start_loc[b + 1])
+        rows.extend(range(s, e))
+        qsl.append(qsl[-1] + e - s)
+    rows = np.array(rows, dtype=np.int64)
+    tables = np.array([[remap[int(x)] if x >= 0 else -1 for x in bt.block_tables[b]] for b in seqs], dtype=np.int32)
+    slots = bt.slot_mapping[rows]
+    new_slots = np.array([remap[int(s) // 16] * 16 + int(s) % 16 if s >= 0 else -1 for s in slots], dtype=np.int64)
+    return W.Batch(name=bt.name + f"-sample{len(seqs)}", q=bt.q[rows], k=bt.k[rows], v=bt.v[rows],
+                   positions=bt.positions[rows], slot_mapping=new_slots, k_cache=bt.k_cache[idx],
+                   v_cache=bt.v_cache[idx], block_tables=tables, context_lens=bt.context_lens[seqs],
+                   query_start_loc=np.array(qsl, dtype=np.int32), scale=bt.scale, rope_theta=bt.rope_theta)
+
+
+def oracle_step(sb):
+    import oracle
+
+    q_rot, kc, vc = oracle.kv_append(sb.q, sb.k, sb.v, sb.positions, sb.slot_mapping, sb.k_cache,
+                                     sb.v_cache, sb.rope_theta)
+    return oracle.paged_attention(q_rot, kc, vc, sb.block_tables, sb.context_lens, sb.query_start_loc,
+                                  sb.scale)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def time_oracle(bt, budget_s=12.0, min_seqs=2):
+    """Time the oracle on the first n sequences, n grown until a step costs ~budget/4."""
+    n = min_seqs
+    while True:
+        sb = sub_batch(bt, range(n))
+        t0 = time.perf_counter()
+        oracle_step(sb)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or n >= bt.num_seqs:
+            return sb, dt, n
+        n = min(bt.num_seqs, max(n + 1, int(n * min(8.0, (budget_s / 4) / max(dt, 1e-3)))))
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="pkv_clocks_", suffix=".csv")
+            f = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ peaks
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_traffic(bt_name, algorithmic_bytes):
+    """Per-launch DRAM traffic of the decode kernel from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for name in rec.get("sources", []):
+        with open(os.path.join(ROOT, name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("source_sha256"):
+        return None
+    entry = rec.get("workloads", {}).get(bt_name)
+    if not entry:
+        return None
+    return float(entry["dram_bytes_per_launch"])
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    from paged_kv_gqa_14_gb300 import build as B
+    from paged_kv_gqa_14_gb300 import ops
+
+    B.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    bt = W.config(args.workload, poison=False)
+    kv_u = kv_unique_bytes(bt)
+    kv_l = kv_logical_bytes(bt)
+    algo = decode_algorithmic_bytes(bt, kv_u)
+    n_decode = int((np.diff(bt.query_start_loc) == 1).sum())
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q0 = up(bt.q)
+    q = q0.clone()
+    k, v = up(bt.k), up(bt.v)
+    kc, vc = up(bt.k_cache), up(bt.v_cache)
+    pos = torch.from_numpy(bt.positions).to(dev)
+    slots = torch.from_numpy(bt.slot_mapping).to(dev)
+    tables = torch.from_numpy(bt.block_tables).to(dev)
+    ctx = torch.from_numpy(bt.context_lens).to(dev)
+    qsl = torch.from_numpy(bt.query_start_loc).to(dev)
+    out = torch.empty_like(q)
+    ws = ops.alloc_workspace(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
+                             bt.block_tables.shape[1], device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ops.kv_append(q, k, v, pos, slots, kc, vc, bt.rope_theta)
+        ops.paged_attention(q, kc, vc, tables, ctx, qsl, bt.scale, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0, "device error during warm-up"
+
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    dec = [(ev(), ev()) for _ in range(K)]
+    app = [(ev(), ev()) for _ in range(K)]
+    att0 = [ev() for _ in range(K)]
+    att1 = [ev() for _ in range(K)]
+    scratch = [ev() for _ in range(K)]
+    t_start, t_stop = ev(), ev()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        ops.set_kernel_events("decode", *dec[i])
+        ops.set_kernel_events("kv_append", *app[i])
+        ops.set_kernel_events("plan", att0[i], scratch[i])
+        ops.set_kernel_events("merge", scratch[i], att1[i])
+        step()
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ops.set_kernel_events("decode")
+    ops.set_kernel_events("kv_append")
+    ops.set_kernel_events("plan")
+    ops.set_kernel_events("merge")
+    total_ms = t_start.elapsed_time(t_stop)
+    dec_ms = [a.elapsed_time(b) for a, b in dec]
+    app_ms = [a.elapsed_time(b) for a, b in app]
+    att_ms = [a.elapsed_time(b) for a, b in zip(att0, att1)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / K
+    dec_avg = sum(dec_ms) / K
+    peak, peak_kind = hbm_peak()
+    achieved = algo / (dec_avg * 1e-3) / 1e9
+    traffic = decode_traffic(bt.name, algo)
+
+    # end to end through the public API with host buffers: pinned inputs -> device, step,
+    # result -> pinned host, every step
+    host_in = {
+        "q": torch.from_numpy(bt.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "k": torch.from_numpy(bt.k.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "v": torch.from_numpy(bt.v.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "pos": torch.from_numpy(bt.positions).pin_memory(),
+        "slots": torch.from_numpy(bt.slot_mapping).pin_memory(),
+        "tables": torch.from_numpy(bt.block_tables).pin_memory(),
+        "ctx": torch.from_numpy(bt.context_lens).pin_memory(),
+        "qsl": torch.from_numpy(bt.query_start_loc).pin_memory(),
+    }
+    dev_in = {"q": q, "k": k, "v": v, "pos": pos, "slots": slots, "tables": tables, "ctx": ctx, "qsl": qsl}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for name, t in host_in.items():
+            dev_in[name].copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    if dist:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert ops.get_device_error() == 0, "device error during timing"
+
+    line = {
+        "metric": METRIC,
+        "value": round(world * kv_u / (ms_step * 1e-3) / 1e9, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": bt.name,
+            "num_seqs": bt.num_seqs,
+            "num_q_heads": bt.num_q_heads,
+            "num_kv_heads": bt.num_kv_heads,
+            "head_dim": bt.head_dim,
+            "block_size": 16,
+            "context_lens": [int(bt.context_lens.min()), int(bt.context_lens.max())],
+            "num_blocks": bt.num_blocks,
+            "new_tokens": bt.num_tokens,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (unique KV per step %.0f MB > 129 MB); no flush" % (kv_u / 1e6),
+        },
+        "tokens_per_s_per_layer": round(world * bt.num_tokens / (ms_step * 1e-3), 1),
+        "kv_unique_bytes": kv_u,
+        "kv_logical_bytes": kv_l,
+        "kv_logical_gbs": round(world * kv_l / (ms_step * 1e-3) / 1e9, 2),
+        "hbm_frac_step": round(kv_u / (ms_step * 1e-3) / 1e9 / peak, 4),
+        "kernels_ms": {
+            "kv_append": round(sum(app_ms) / K, 5),
+            "paged_attention_call": round(sum(att_ms) / K, 5),
+            "decode_splitk": round(dec_avg, 5),
+        },
+        "roofline": {
+            "kernel": "decode_splitk",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes": algo,
+        },
+        "e2e": {
+            "value": round(world * kv_u / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": UNIT,
+            "ms_per_step": round(e2e_ms, 5),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": 5 * K,
+        "clocks": clk,
+        "decode_seqs": n_decode,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        sb, dt, n = time_oracle(bt, budget_s=args.cpu_budget)
+        kv_s = kv_unique_bytes(sb)
+        line["cpu_baseline"] = {
+            "value": round(kv_s / dt / 1e9, 4),
+            "unit": UNIT,
+            "cores": host_cores(),
+            "kind": "oracle",
+            "sample": f"first {n} of {bt.num_seqs} sequences of {bt.name} ({kv_s / 1e6:.1f} MB unique KV), "
+                      f"oracle kv_append + paged_attention, one pass {dt:.2f} s",
+        }
+    if dist:
+        dist.destroy_process_group()
+    return line
+
+
+# ----------------------------------------------------------------------- reference arm
+def run_reference(args):
+    bt = W.config(args.workload, poison=False)
+    sb, dt, n = time_oracle(bt, budget_s=min(args.cpu_budget, 8.0))
+    kv_s = kv_unique_bytes(sb)
+    for _ in range(args.warmup):
+        oracle_step(sb)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(sb)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = round(kv_s / (ms * 1e-3) / 1e9, 4)
+    return {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "impl": "reference",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": bt.name, "sample_seqs": n, "num_seqs": bt.num_seqs},
+        "cpu_baseline": {
+            "value": value,
+            "unit": UNIT,
+            "cores": host_cores(),
+            "kind": "oracle",
+            "sample": f"first {n} of {bt.num_seqs} sequences of {bt.name} per step ({kv_s / 1e6:.1f} MB unique KV)",
+        },
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        line = run_reference(args)
+    else:
+        line = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

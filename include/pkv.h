@@ -1,0 +1,200 @@
+/*
+ * pkv.h -- C ABI of the paged-KV grouped-query attention library for GB300 (sm_103a).
+ *
+ * Two operations make up one attention layer's step of a continuous-batching, paged-KV
+ * serving engine:
+ *
+ *   pkv_kv_append        fused RoPE + KV-cache write of the step's new tokens
+ *                        ("mini_engine" README, "Next: fused kernels": fused RoPE, fused QKV
+ *                        split and KV-cache write; "09 -- Mini Inference Engine (The
+ *                        Capstone)", "Week 4 -- Paged KV cache": pool of 16-token blocks).
+ *   pkv_paged_attention  grouped-query attention of every new token over its sequence's
+ *                        paged context, decode tokens and causal prefill chunks mixed in one
+ *                        call ("mini_engine" README, "What it does": GQA, paged KV cache,
+ *                        chunked prefill; "09 -- ...", "Week 3 -- Continuous batching":
+ *                        mixed prefill/decode batches with varying lengths; "Week 4":
+ *                        attention that gathers through the block table).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named *_dev are CUDA device pointers; the library never dereferences them on
+ *    the host.  All tensors are owned by the caller; the library allocates no device memory
+ *    (scratch space comes from the caller's workspace), never synchronises, and enqueues its
+ *    kernels asynchronously on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *    default stream).  Every call works on the device that is current on the calling thread.
+ *  - bf16 tensors hold IEEE bfloat16 values.  The last dimension (head_dim) is contiguous;
+ *    other strides are in ELEMENTS.  Every row of head_dim elements must start on a 16-byte
+ *    boundary (base pointers 16-byte aligned, strides multiples of 8 elements).
+ *  - KV pool layout (per layer): k_cache and v_cache are each a contiguous bf16 tensor
+ *    [num_blocks][block_size][num_kv_heads][head_dim] with block_size = 16.  Slot s denotes
+ *    row (s % 16) of physical block (s / 16).
+ *  - q head h attends with kv head h / (num_q_heads / num_kv_heads).
+ *  - RoPE is the rotate-half form: pair (i, i + d/2) turns by pos * theta^(-2i/d).
+ *  - Return value: PKV_OK, or a PKV_ERR_* code.  On a host-side validation error nothing is
+ *    launched.  No C++ exception crosses this boundary.
+ *  - Data-dependent index errors (a slot or block id outside the pool, a context longer than
+ *    its block-table row, a malformed query_start_loc) are detected on the device: the
+ *    offending access is skipped (or redirected to block 0), the affected output is
+ *    unspecified, and a bit is or-ed into a per-device error word that
+ *    pkv_get_device_error() reads.  Kernels never trap.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes returned by every entry point ---- */
+#define PKV_OK 0
+#define PKV_ERR_NULL 1        /* a required pointer is NULL                                   */
+#define PKV_ERR_SHAPE 2       /* a size is negative or sizes disagree                          */
+#define PKV_ERR_STRIDE 3      /* a stride is not allowed (overlapping rows, non-contiguous pool) */
+#define PKV_ERR_ALIGN 4       /* a pointer or stride breaks the 16-byte row alignment           */
+#define PKV_ERR_UNSUPPORTED 5 /* head_dim / block_size / head counts outside the compiled set   */
+#define PKV_ERR_WORKSPACE 6   /* workspace NULL, misaligned (256 B) or smaller than required    */
+#define PKV_ERR_CUDA 7        /* a CUDA runtime call or kernel launch failed                    */
+
+/* ---- device-side error bits (pkv_get_device_error) ---- */
+#define PKV_DEVERR_SLOT_RANGE 0x1u  /* kv_append: slot >= num_blocks*16; that write was skipped     */
+#define PKV_DEVERR_BLOCK_RANGE 0x2u /* attention: block id outside [0, num_blocks); read block 0  */
+#define PKV_DEVERR_SPAN 0x4u        /* attention: query_start_loc not monotone, past num_tokens,
+                                       or context shorter than the span; sequence skipped        */
+#define PKV_DEVERR_CONTEXT 0x8u     /* attention: context > max_blocks_per_seq*16; seq skipped     */
+#define PKV_DEVERR_TIMEOUT 0x10u    /* a bounded wait inside a kernel ran out; output unspecified */
+
+/* Supported sizes (compiled set). */
+#define PKV_BLOCK_SIZE 16
+
+/* Human-readable name of a status code (static string, never NULL). */
+PKV_API const char* pkv_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+PKV_API int pkv_version(void);
+
+/*
+ * pkv_kv_append -- fused RoPE and KV-cache append for the step's new tokens.
+ *
+ * For each new token t in [0, num_tokens):
+ *   q[t, h, :]   <- bf16(rope(q[t, h, :], positions[t]))            for every q head (in place)
+ *   if slot_mapping[t] >= 0, with s = slot_mapping[t]:
+ *     k_cache[s/16, s%16, h, :] <- bf16(rope(k[t, h, :], positions[t]))   for every kv head
+ *     v_cache[s/16, s%16, h, :] <- v[t, h, :]                              (bit copy)
+ * Rotation: fp32 arithmetic on an angle reduced in fp64; rounding to bf16 nearest-even.
+ * A negative slot marks padding and writes nothing.  A slot >= num_blocks*16 is skipped
+ * and sets PKV_DEVERR_SLOT_RANGE.  Duplicate slots in one call give an unspecified row.
+ *
+ *   q_dev          bf16 [num_tokens][num_q_heads][head_dim], strides (q_stride_token,
+ *                  q_stride_head); rotated in place.  May alias a packed QKV buffer.
+ *   k_dev, v_dev   bf16 [num_tokens][num_kv_heads][head_dim] with their own strides; read only.
+ *   positions_dev  int64 [num_tokens]: absolute position of each token (>= 0).
+ *   slot_mapping_dev int64 [num_tokens]: destination slot, or < 0 to skip.
+ *   k_cache_dev, v_cache_dev  bf16 pools (layout above) of num_blocks blocks.
+ *   head_dim       64 or 128.   block_size  must be 16.
+ *   rope_theta     RoPE base (> 0), e.g. 1e6 for Qwen3.
+ * num_tokens == 0 is a no-op returning PKV_OK.
+ */
+PKV_API int pkv_kv_append(void* q_dev, int64_t q_stride_token, int64_t q_stride_head,
+                  const void* k_dev, int64_t k_stride_token, int64_t k_stride_head,
+                  const void* v_dev, int64_t v_stride_token, int64_t v_stride_head,
+                  const int64_t* positions_dev, const int64_t* slot_mapping_dev,
+                  void* k_cache_dev, void* v_cache_dev,
+                  int64_t num_tokens, int64_t num_q_heads, int64_t num_kv_heads,
+                  int64_t head_dim, int64_t num_blocks, int64_t block_size,
+                  double rope_theta, void* stream);
+
+/*
+ * pkv_paged_attention_workspace_size -- bytes of device workspace pkv_paged_attention needs
+ * for these sizes on the current device (the split-K partials and the work plan).
+ * Returns 0 if the sizes are invalid.  The result depends on the device's SM count and on
+ * pkv_set_decode_ctas(); call it on the device that will run the attention.
+ */
+PKV_API size_t pkv_paged_attention_workspace_size(int64_t num_tokens, int64_t num_seqs,
+                                          int64_t num_q_heads, int64_t num_kv_heads,
+                                          int64_t head_dim, int64_t max_blocks_per_seq);
+
+/*
+ * pkv_paged_attention -- grouped-query attention over a ragged batch of paged sequences.
+ *
+ * Sequence b owns query rows [query_start_loc[b], query_start_loc[b+1]) (its span, n rows)
+ * and context_lens[b] keys (ctx, counting the span's own tokens, which kv_append has already
+ * written).  Its keys live in physical blocks block_tables[b, 0 .. ceil(ctx/16)-1].
+ * Row r of the span is the token at position ctx - n + r; for every q head h:
+ *     out[row, h, :] = softmax_j(scale * q[row, h, :] . K[j, h/G, :]) V[j, h/G, :],
+ *     j over keys 0 .. ctx - n + r           (G = num_q_heads / num_kv_heads)
+ * A span of one row is a decode step and sees the whole context; longer spans are causal
+ * chunked-prefill spans.  Accumulation is fp32; out is rounded to bf16 nearest-even.
+ * Rows of out outside every span are not written.  Spans may be empty.
+ *
+ *   q_dev            bf16 [num_tokens][num_q_heads][head_dim] (already rotated), strides as given.
+ *   k_cache_dev, v_cache_dev  the pool (layout above), num_blocks blocks of block_size 16.
+ *   block_tables_dev int32 [num_seqs][block_tables_stride]; only the first
+ *                    ceil(ctx/16) <= max_blocks_per_seq entries of row b are read.
+ *   context_lens_dev int32 [num_seqs].
+ *   query_start_loc_dev int32 [num_seqs + 1], non-decreasing, [0] = 0, [num_seqs] <= num_tokens.
+ *   out_dev          bf16 [num_tokens][num_q_heads][head_dim], strides as given; must not
+ *                    overlap q.
+ *   scale            softmax scale (typically 1/sqrt(head_dim)).
+ *   workspace_dev    >= pkv_paged_attention_workspace_size(...) bytes, 256-byte aligned,
+ *                    owned by the caller, used as scratch; its contents need no
+ *                    initialisation and are clobbered.  Calls that share a workspace
+ *                    must be stream-ordered.
+ * Supported: head_dim in {64, 128}; num_kv_heads in {1, 2, 4, 8};
+ *            num_q_heads / num_kv_heads in [1, 8].
+ */
+PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64_t q_stride_head,
+                        const void* k_cache_dev, const void* v_cache_dev,
+                        int64_t num_blocks, int64_t block_size,
+                        const int32_t* block_tables_dev, int64_t block_tables_stride,
+                        int64_t max_blocks_per_seq,
+                        const int32_t* context_lens_dev, const int32_t* query_start_loc_dev,
+                        int64_t num_seqs,
+                        void* out_dev, int64_t out_stride_token, int64_t out_stride_head,
+                        int64_t num_tokens, int64_t num_q_heads, int64_t num_kv_heads,
+                        int64_t head_dim, float scale,
+                        void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_set_decode_ctas -- override the number of CTAs the decode split-K kernel uses
+ * (0 = automatic: one per SM).  Process-wide; meant for tests and tuning.  Changes the
+ * split points, hence rounding, never the result beyond fp32 rounding.  Returns PKV_OK,
+ * or PKV_ERR_SHAPE for a negative value.
+ */
+PKV_API int pkv_set_decode_ctas(int32_t ctas);
+
+/*
+ * pkv_set_kernel_events -- instrumentation: from now on, every launch of kernel `which`
+ * records `start_event` on its stream just before the launch and `stop_event` just after
+ * (both cudaEvent_t passed as void*, created by the caller).  NULL events (or which = 0)
+ * switch recording off for that kernel.  Process-wide; meant for benchmarks that time one
+ * kernel inside a call.  Returns PKV_ERR_SHAPE for an unknown `which`.
+ *   which: 1 kv_append, 2 planner, 3 prefill tiles, 4 decode split-K, 5 split merge.
+ */
+#define PKV_KERNEL_APPEND 1
+#define PKV_KERNEL_PLAN 2
+#define PKV_KERNEL_PREFILL 3
+#define PKV_KERNEL_DECODE 4
+#define PKV_KERNEL_MERGE 5
+PKV_API int pkv_set_kernel_events(int which, void* start_event, void* stop_event);
+
+/*
+ * pkv_get_device_error -- read the current device's error word (PKV_DEVERR_* bits or-ed
+ * together since the last clear) into *bits, after synchronising `stream`.  If clear != 0
+ * the word is reset to zero.  This call blocks the host; the others never do.
+ */
+PKV_API int pkv_get_device_error(uint32_t* bits, int clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,338 @@
+// paged_attention: work planner, decode split-K, prefill-chunk tiles and split merge.
+//
+// Launch sequence on the caller's stream (no host synchronisation; every grid size comes
+// from tensor shapes only):
+//   1. plan_kernel      (1 CTA)   classify spans, build the decode unit ranges and the
+//                                 prefill tile list in the workspace
+//   2. prefill kernel   (persistent) causal varlen tiles for spans longer than one row
+//   3. decode kernel    (1 CTA/SM) split-K over page groups for spans of one row
+//   4. merge_kernel     (B CTAs)  combine the split states of sequences cut by a CTA boundary
+#include "decode.cuh"
+#include "prefill.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+struct Int3 {
+  int a, b, c;
+};
+
+// Block-wide exclusive scan of three counters at once.  `tot` receives the block totals.
+__device__ Int3 block_scan3(Int3 v, Int3& tot, int* sm /* [3 * 32] */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  Int3 x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, x.a, off);
+    const int yb = __shfl_up_sync(0xffffffffu, x.b, off);
+    const int yc = __shfl_up_sync(0xffffffffu, x.c, off);
+    if (lane >= off) {
+      x.a += ya;
+      x.b += yb;
+      x.c += yc;
+    }
+  }
+  if (lane == 31) {
+    sm[warp * 3 + 0] = x.a;
+    sm[warp * 3 + 1] = x.b;
+    sm[warp * 3 + 2] = x.c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    Int3 w = {0, 0, 0};
+    if (lane < nwarps) w = {sm[lane * 3], sm[lane * 3 + 1], sm[lane * 3 + 2]};
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int ya = __shfl_up_sync(0xffffffffu, w.a, off);
+      const int yb = __shfl_up_sync(0xffffffffu, w.b, off);
+      const int yc = __shfl_up_sync(0xffffffffu, w.c, off);
+      if (lane >= off) {
+        w.a += ya;
+        w.b += yb;
+        w.c += yc;
+      }
+    }
+    if (lane < nwarps) {
+      sm[lane * 3 + 0] = w.a;
+      sm[lane * 3 + 1] = w.b;
+      sm[lane * 3 + 2] = w.c;
+    }
+  }
+  __syncthreads();
+  Int3 base = {0, 0, 0};
+  if (warp > 0) base = {sm[(warp - 1) * 3], sm[(warp - 1) * 3 + 1], sm[(warp - 1) * 3 + 2]};
+  tot = {sm[(nwarps - 1) * 3], sm[(nwarps - 1) * 3 + 1], sm[(nwarps - 1) * 3 + 2]};
+  __syncthreads();
+  return {base.a + x.a - v.a, base.b + x.b - v.b, base.c + x.c - v.c};
+}
+
+// Span classification and work lists ("09 -- Mini Inference Engine (The Capstone)",
+// "Week 3 -- Continuous batching": prefill and decode sequences mixed in one batch).
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ qsl,
+                                                            const int32_t* __restrict__ ctxl,
+                                                            int num_seqs, int64_t num_tokens,
+                                                            int64_t max_blocks, int pps,
+                                                            int decode_ctas, Plan plan,
+                                                            int64_t max_tiles, unsigned int* err) {
+  __shared__ int sm[3 * 32];
+  __shared__ int carry[3];
+  if (threadIdx.x == 0) carry[0] = carry[1] = carry[2] = 0;
+  __syncthreads();
+  for (int base = 0; base < num_seqs; base += kPlanThreads) {
+    const int b = base + threadIdx.x;
+    Int3 v = {0, 0, 0};
+    if (b < num_seqs) {
+      const int s0 = qsl[b], s1 = qsl[b + 1];
+      const int ctx = ctxl[b];
+      const int span = s1 - s0;
+      bool ok = s0 >= 0 && span >= 0 && s1 <= num_tokens;
+      if (!ok) {
+        raise_error(err, PKV_DEVERR_SPAN);
+      } else if (span > 0) {
+        if (ctx < span) {
+          raise_error(err, PKV_DEVERR_SPAN);
+          ok = false;
+        } else if (static_cast<int64_t>(ctx) > max_blocks * kBlockSize) {
+          raise_error(err, PKV_DEVERR_CONTEXT);
+          ok = false;
+        }
+      }
+      if (ok && span == 1) {
+        v.a = 1;
+        v.b = ceil_div(ceil_div(ctx, kBlockSize), pps);
+      }
+      if (ok && span > 1) v.c = ceil_div(span, kPrefillTileQ);
+    }
+    Int3 tot;
+    Int3 ex = block_scan3(v, tot, sm);
+    ex.a += carry[0];
+    ex.b += carry[1];
+    ex.c += carry[2];
+    if (v.a) {
+      plan.dec_seq[ex.a] = b;
+      plan.dec_unit[ex.a] = ex.b;
+    }
+    for (int j = 0; j < v.c; ++j) {
+      if (ex.c + j < max_tiles) {
+        plan.pf_seq[ex.c + j] = b;
+        plan.pf_tile[ex.c + j] = j;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      carry[0] += tot.a;
+      carry[1] += tot.b;
+      carry[2] += tot.c;
+    }
+    __syncthreads();
+  }
+  const int n_dec = carry[0];
+  const int U = carry[1];
+  const int n_tiles = static_cast<int>(min(static_cast<int64_t>(carry[2]), max_tiles));
+  const int W = max(1, ceil_div(U, decode_ctas));
+  if (threadIdx.x == 0) plan.dec_unit[n_dec] = U;
+  __syncthreads();
+
+  // split pieces per decode sequence and the first partial slot of each
+  __shared__ int carry2;
+  if (threadIdx.x == 0) carry2 = 0;
+  __syncthreads();
+  for (int base = 0; base < n_dec; base += kPlanThreads) {
+    const int i = base + threadIdx.x;
+    Int3 v = {0, 0, 0};
+    if (i < n_dec) {
+      const int u0 = plan.dec_unit[i], u1 = plan.dec_unit[i + 1];
+      v.a = (u1 - 1) / W - u0 / W + 1;
+    }
+    Int3 tot;
+    const Int3 ex = block_scan3(v, tot, sm);
+    if (i < n_dec) {
+      plan.dec_slot[i] = ex.a + carry2;
+      plan.dec_chunks[i] = v.a;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry2 += tot.a;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    plan.header[0] = n_dec;
+    plan.header[1] = U;
+    plan.header[2] = W;
+    plan.header[3] = n_tiles;
+    plan.header[4] = carry2;
+  }
+}
+
+// Merge the split states of each decode sequence cut by a CTA boundary:
+// out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k  (scores are in the log2 domain).
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(Plan plan, const int32_t* __restrict__ qsl,
+                                                    bf16* __restrict__ out, int64_t o_st,
+                                                    int64_t o_sh, int hq) {
+  const int i = blockIdx.x;
+  if (i >= plan.header[0]) return;
+  const int chunks = plan.dec_chunks[i];
+  if (chunks <= 1) return;
+  const int slot0 = plan.dec_slot[i];
+  const int64_t t = qsl[plan.dec_seq[i]];
+  constexpr int V = 4;  // dims per thread
+  for (int item = threadIdx.x; item < hq * (D / V); item += blockDim.x) {
+    const int h = item / (D / V);
+    const int d0 = (item - h * (D / V)) * V;
+    float M = -__int_as_float(0x7f800000);
+    for (int k = 0; k < chunks; ++k)
+      M = fmaxf(M, plan.part_ml[(static_cast<int64_t>(slot0 + k) * hq + h) * 2]);
+    float num[V] = {0.f, 0.f, 0.f, 0.f};
+    float den = 0.f;
+    for (int k = 0; k < chunks; ++k) {
+      const int64_t sh = static_cast<int64_t>(slot0 + k) * hq + h;
+      const float2 ml = *reinterpret_cast<const float2*>(plan.part_ml + sh * 2);
+      const float w = fast_exp2(ml.x - M);
+      den = fmaf(w, ml.y, den);
+      const float4 a = *reinterpret_cast<const float4*>(plan.part_acc + sh * D + d0);
+      num[0] = fmaf(w, a.x, num[0]);
+      num[1] = fmaf(w, a.y, num[1]);
+      num[2] = fmaf(w, a.z, num[2]);
+      num[3] = fmaf(w, a.w, num[3]);
+    }
+    const float inv = 1.f / den;
+    uint2 o;
+    o.x = pack_bf16x2(num[0] * inv, num[1] * inv);
+    o.y = pack_bf16x2(num[2] * inv, num[3] * inv);
+    *reinterpret_cast<uint2*>(out + t * o_st + h * o_sh + d0) = o;
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
+  using C = DecodeCfg<D, G>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_splitk_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  DecodeParams p;
+  p.q = static_cast<const bf16*>(a.q);
+  p.q_st = a.q_st;
+  p.q_sh = a.q_sh;
+  p.k_cache = static_cast<const bf16*>(a.k_cache);
+  p.v_cache = static_cast<const bf16*>(a.v_cache);
+  p.num_blocks = a.num_blocks;
+  p.block_tables = a.block_tables;
+  p.bt_stride = a.bt_stride;
+  p.context_lens = a.context_lens;
+  p.qsl = a.qsl;
+  p.out = static_cast<bf16*>(a.out);
+  p.o_st = a.o_st;
+  p.o_sh = a.o_sh;
+  p.hkv = a.hkv;
+  p.hq = a.hq;
+  p.qscale = a.scale * 1.4426950408889634f;
+  p.plan = a.plan;
+  p.err = a.err;
+  record_kernel_event(PKV_KERNEL_DECODE, false, stream);
+  decode_splitk_kernel<D, G><<<a.decode_ctas, (kDecodeWarps + 1) * 32, C::kSmemBytes, stream>>>(p);
+  record_kernel_event(PKV_KERNEL_DECODE, true, stream);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_g(const AttnArgs& a, cudaStream_t stream) {
+  switch (a.hq / a.hkv) {
+    case 1: return launch_decode<D, 1>(a, stream);
+    case 2: return launch_decode<D, 2>(a, stream);
+    case 3: return launch_decode<D, 3>(a, stream);
+    case 4: return launch_decode<D, 4>(a, stream);
+    case 5: return launch_decode<D, 5>(a, stream);
+    case 6: return launch_decode<D, 6>(a, stream);
+    case 7: return launch_decode<D, 7>(a, stream);
+    case 8: return launch_decode<D, 8>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.num_tokens == 0) return cudaSuccess;
+  const int pps = kDecodeWarps / a.hkv;
+  record_kernel_event(PKV_KERNEL_PLAN, false, stream);
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.qsl, a.context_lens, static_cast<int>(a.num_seqs),
+                                               a.num_tokens, a.max_blocks, pps, a.decode_ctas, a.plan,
+                                               a.max_tiles, a.err);
+  record_kernel_event(PKV_KERNEL_PLAN, true, stream);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = (a.head_dim == 128) ? launch_prefill<128>(a, stream) : launch_prefill<64>(a, stream);
+  if (e != cudaSuccess) return e;
+  e = (a.head_dim == 128) ? launch_decode_g<128>(a, stream) : launch_decode_g<64>(a, stream);
+  if (e != cudaSuccess) return e;
+  const dim3 mgrid(static_cast<unsigned>(a.num_seqs));
+  record_kernel_event(PKV_KERNEL_MERGE, false, stream);
+  if (a.head_dim == 128)
+    merge_kernel<128><<<mgrid, 256, 0, stream>>>(a.plan, a.qsl, static_cast<bf16*>(a.out), a.o_st, a.o_sh, a.hq);
+  else
+    merge_kernel<64><<<mgrid, 256, 0, stream>>>(a.plan, a.qsl, static_cast<bf16*>(a.out), a.o_st, a.o_sh, a.hq);
+  record_kernel_event(PKV_KERNEL_MERGE, true, stream);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ workspace layout
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+PlanSizes plan_sizes(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
+                     int64_t decode_ctas) {
+  PlanSizes s{};
+  s.num_seqs = num_seqs;
+  s.num_tokens = num_tokens;
+  s.num_q_heads = num_q_heads;
+  s.head_dim = head_dim;
+  s.decode_ctas = decode_ctas;
+  s.max_tiles = num_tokens / kPrefillTileQ + num_seqs + 1;
+  s.max_slots = num_seqs + decode_ctas;
+  size_t off = 0;
+  s.off_header = off;
+  off = align256(off + 16 * sizeof(int));
+  s.off_dec_seq = off;
+  off = align256(off + num_seqs * sizeof(int));
+  s.off_dec_unit = off;
+  off = align256(off + (num_seqs + 1) * sizeof(int));
+  s.off_dec_slot = off;
+  off = align256(off + num_seqs * sizeof(int));
+  s.off_dec_chunks = off;
+  off = align256(off + num_seqs * sizeof(int));
+  s.off_pf_seq = off;
+  off = align256(off + s.max_tiles * sizeof(int));
+  s.off_pf_tile = off;
+  off = align256(off + s.max_tiles * sizeof(int));
+  s.off_part_ml = off;
+  off = align256(off + s.max_slots * num_q_heads * 2 * sizeof(float));
+  s.off_part_acc = off;
+  off = align256(off + s.max_slots * num_q_heads * head_dim * sizeof(float));
+  s.total = off;
+  return s;
+}
+
+Plan plan_view(void* workspace, const PlanSizes& s) {
+  char* w = static_cast<char*>(workspace);
+  Plan p;
+  p.header = reinterpret_cast<int*>(w + s.off_header);
+  p.dec_seq = reinterpret_cast<int*>(w + s.off_dec_seq);
+  p.dec_unit = reinterpret_cast<int*>(w + s.off_dec_unit);
+  p.dec_slot = reinterpret_cast<int*>(w + s.off_dec_slot);
+  p.dec_chunks = reinterpret_cast<int*>(w + s.off_dec_chunks);
+  p.pf_seq = reinterpret_cast<int*>(w + s.off_pf_seq);
+  p.pf_tile = reinterpret_cast<int*>(w + s.off_pf_tile);
+  p.part_ml = reinterpret_cast<float*>(w + s.off_part_ml);
+  p.part_acc = reinterpret_cast<float*>(w + s.off_part_acc);
+  return p;
+}
+
+}  // namespace pkv

@@ -1,0 +1,100 @@
+// Internal interface between the C entry points (abi.cu) and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;       // tokens per KV block (the pool's block_size)
+constexpr int kDecodeWarps = 8;      // consumer warps of the decode split-K kernel
+constexpr int kPrefillTileQ = 64;    // query rows per prefill work tile
+constexpr int kMaxHeadDim = 128;
+
+// ---------------------------------------------------------------- work plan layout
+// The planner kernel fills these arrays in the caller's workspace; the decode, prefill
+// and merge kernels read them.  All offsets are 256-byte aligned.
+//
+// header[0] number of decode sequences (span == 1)            n_dec
+// header[1] total decode work units                            U
+// header[2] work units per decode CTA                          W = ceil(U / C)
+// header[3] number of prefill (seq, q-tile) work items         n_tiles
+// header[4] partial-result slots in use                        S
+//
+// A decode work unit is one page group of one sequence: P = kDecodeWarps / Hkv
+// consecutive 16-token pages, all kv heads.  Decode CTA c owns units [c W, (c+1) W) of
+// the concatenation of all decode sequences' units.
+struct Plan {
+  int* header;      // [16]
+  int* dec_seq;     // [B]      decode list: sequence id
+  int* dec_unit;    // [B + 1]  exclusive prefix of work units over the decode list
+  int* dec_slot;    // [B]      first partial slot of each decode sequence
+  int* dec_chunks;  // [B]      number of decode CTAs that touch the sequence
+  int* pf_seq;      // [max_tiles]  prefill work item: sequence id
+  int* pf_tile;     // [max_tiles]  prefill work item: q-tile index within the span
+  float* part_ml;   // [S_max][Hq][2]   split state: running max (log2 domain), sum of weights
+  float* part_acc;  // [S_max][Hq][D]   split state: unnormalised weighted sum of V
+};
+
+struct PlanSizes {
+  int64_t num_seqs, num_tokens, num_q_heads, head_dim, decode_ctas;
+  int64_t max_tiles, max_slots;
+  size_t off_header, off_dec_seq, off_dec_unit, off_dec_slot, off_dec_chunks;
+  size_t off_pf_seq, off_pf_tile, off_part_ml, off_part_acc, total;
+};
+
+PlanSizes plan_sizes(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
+                     int64_t decode_ctas);
+Plan plan_view(void* workspace, const PlanSizes& s);
+
+// ------------------------------------------------------------------------ launchers
+struct AppendArgs {
+  void* q;
+  int64_t q_st, q_sh;
+  const void* k;
+  int64_t k_st, k_sh;
+  const void* v;
+  int64_t v_st, v_sh;
+  const int64_t* positions;
+  const int64_t* slots;
+  void* k_cache;
+  void* v_cache;
+  int64_t num_tokens, num_slots;
+  int hq, hkv, head_dim;
+  double theta;
+  unsigned int* err;
+};
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+
+struct AttnArgs {
+  const void* q;
+  int64_t q_st, q_sh;
+  const void* k_cache;
+  const void* v_cache;
+  int64_t num_blocks;
+  const int32_t* block_tables;
+  int64_t bt_stride, max_blocks;
+  const int32_t* context_lens;
+  const int32_t* qsl;
+  int64_t num_seqs;
+  void* out;
+  int64_t o_st, o_sh;
+  int64_t num_tokens;
+  int hq, hkv, head_dim;
+  float scale;
+  int decode_ctas;
+  Plan plan;
+  int64_t max_tiles;
+  unsigned int* err;
+};
+cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream);
+
+int device_sm_count();
+
+// Records the caller's timing event around a kernel launch when one is registered
+// (pkv_set_kernel_events); `after` selects the stop event.
+void record_kernel_event(int which, bool after, cudaStream_t stream);
+int decode_ctas_for_device();
+
+}  // namespace pkv

@@ -1,0 +1,129 @@
+// Fused RoPE + KV-cache append ("mini_engine" README, "Next: fused kernels": fused RoPE
+// and fused QKV split + KV-cache write; "09 -- Mini Inference Engine (The Capstone)",
+// "Week 4 -- Paged KV cache": pool of 16-token blocks addressed by slot).
+//
+// One CTA per new token.  The token's d/2 rotation angles are computed once into shared
+// memory: angle = pos * f_i with f_i = theta^(-2i/d) (fp64 on the host), reduced to
+// [-pi, pi] in fp64, then sincosf in fp32.  Every head of q (in place) and k (into the
+// slot) is rotated pairwise (i, i + d/2) in fp32 and rounded to bf16 nearest-even; v is a
+// 16-byte vector copy.  All global accesses are 16-byte vectors along head_dim.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kAppendThreads = 128;
+
+struct RopeFreqs {
+  double f[kMaxHeadDim / 2];  // f_i = theta^(-2 i / d), i < d/2
+};
+
+// 2*pi and 1/(2*pi) rounded to double.
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr double kInvTwoPi = 0.159154943091895335768883763372514;
+
+__device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float2* cs) {
+  uint32_t* a = reinterpret_cast<uint32_t*>(&lo);
+  uint32_t* b = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 c0 = cs[2 * j], c1 = cs[2 * j + 1];
+    const float x0 = bf16lo(a[j]), x1 = bf16hi(a[j]);  // first half, pairs 2j, 2j+1
+    const float y0 = bf16lo(b[j]), y1 = bf16hi(b[j]);  // second half, same pairs
+    a[j] = pack_bf16x2(x0 * c0.x - y0 * c0.y, x1 * c1.x - y1 * c1.y);
+    b[j] = pack_bf16x2(y0 * c0.x + x0 * c0.y, y1 * c1.x + x1 * c1.y);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
+    bf16* __restrict__ q, int64_t q_st, int64_t q_sh, const bf16* __restrict__ k, int64_t k_st,
+    int64_t k_sh, const bf16* __restrict__ v, int64_t v_st, int64_t v_sh,
+    const int64_t* __restrict__ positions, const int64_t* __restrict__ slots,
+    bf16* __restrict__ k_cache, bf16* __restrict__ v_cache, int64_t num_slots, int hq, int hkv,
+    const __grid_constant__ RopeFreqs fr, unsigned int* err) {
+  constexpr int HALF = D / 2;
+  constexpr int CH = HALF / 8;  // 16-byte chunks per half head
+  __shared__ float2 cs[HALF];
+
+  const int64_t t = blockIdx.x;
+  const int64_t pos = positions[t];
+  const int64_t slot = slots[t];
+
+  for (int i = threadIdx.x; i < HALF; i += kAppendThreads) {
+    const double a = static_cast<double>(pos) * fr.f[i];
+    const double n = rint(a * kInvTwoPi);
+    const float r = static_cast<float>(fma(-n, kTwoPi, a));
+    float s, c;
+    sincosf(r, &s, &c);
+    cs[i] = make_float2(c, s);
+  }
+  const bool in_range = slot < num_slots;
+  const bool write_kv = slot >= 0 && in_range;
+  if (!in_range && threadIdx.x == 0) raise_error(err, PKV_DEVERR_SLOT_RANGE);
+  __syncthreads();
+
+  // rotations: q heads in place, k heads into the cache row of `slot`
+  const int n_rot = (hq + (write_kv ? hkv : 0)) * CH;
+  for (int item = threadIdx.x; item < n_rot; item += kAppendThreads) {
+    const int head = item / CH;
+    const int c = item - head * CH;
+    const bf16* src;
+    bf16* dst;
+    if (head < hq) {
+      bf16* row = q + t * q_st + head * q_sh;
+      src = row;
+      dst = row;
+    } else {
+      const int h = head - hq;
+      src = k + t * k_st + h * k_sh;
+      dst = k_cache + (slot * hkv + h) * D;
+    }
+    uint4 lo = *reinterpret_cast<const uint4*>(src + c * 8);
+    uint4 hi = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
+    rotate8(lo, hi, cs + c * 8);
+    *reinterpret_cast<uint4*>(dst + c * 8) = lo;
+    *reinterpret_cast<uint4*>(dst + HALF + c * 8) = hi;
+  }
+
+  // v: plain 16-byte copies
+  if (write_kv) {
+    constexpr int VCH = D / 8;
+    for (int item = threadIdx.x; item < hkv * VCH; item += kAppendThreads) {
+      const int h = item / VCH;
+      const int c = item - h * VCH;
+      const uint4 x = *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8);
+      *reinterpret_cast<uint4*>(v_cache + (slot * hkv + h) * D + c * 8) = x;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
+  if (a.num_tokens == 0) return cudaSuccess;
+  RopeFreqs fr;
+  const int half = a.head_dim / 2;
+  for (int i = 0; i < half; ++i) fr.f[i] = pow(a.theta, -2.0 * i / a.head_dim);
+  for (int i = half; i < kMaxHeadDim / 2; ++i) fr.f[i] = 0.0;
+  const dim3 grid(static_cast<unsigned>(a.num_tokens));
+#define PKV_LAUNCH_APPEND(D)                                                                   \
+  kv_append_kernel<D><<<grid, kAppendThreads, 0, stream>>>(                                    \
+      static_cast<bf16*>(a.q), a.q_st, a.q_sh, static_cast<const bf16*>(a.k), a.k_st, a.k_sh, \
+      static_cast<const bf16*>(a.v), a.v_st, a.v_sh, a.positions, a.slots,                    \
+      static_cast<bf16*>(a.k_cache), static_cast<bf16*>(a.v_cache), a.num_slots, a.hq, a.hkv, \
+      fr, a.err)
+  record_kernel_event(PKV_KERNEL_APPEND, false, stream);
+  if (a.head_dim == 128)
+    PKV_LAUNCH_APPEND(128);
+  else
+    PKV_LAUNCH_APPEND(64);
+  record_kernel_event(PKV_KERNEL_APPEND, true, stream);
+#undef PKV_LAUNCH_APPEND
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

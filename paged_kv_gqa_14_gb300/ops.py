@@ -1,0 +1,155 @@
+"""Python binding with the C-ABI's names: argument marshalling only.
+
+Every function here checks dtypes/devices, turns torch tensors into pointers, sizes and
+element strides, and calls the matching ``pkv_*`` entry point on the current torch CUDA
+stream.  No arithmetic of the path runs in Python or torch: all of it is in the kernels.
+PyTorch supplies device memory (the output and workspace buffers) and the stream.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+BLOCK_SIZE = 16
+
+
+def _stream_ptr(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def _rows(t, name):
+    """(token stride, head stride) of a [T, H, d] tensor whose last dim is contiguous."""
+    if t.stride(2) != 1:
+        raise ValueError(f"{name}: head_dim must be contiguous")
+    return t.stride(0), t.stride(1)
+
+
+def _contig1(t, name):
+    if t.dim() != 1 or (t.numel() > 1 and t.stride(0) != 1):
+        raise ValueError(f"{name} must be a contiguous 1-D tensor")
+
+
+def kv_append(q, k, v, positions, slot_mapping, k_cache, v_cache, rope_theta, stream=None):
+    """Fused RoPE + KV append (``pkv_kv_append``).  q is rotated in place."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(positions, "positions", torch.int64, 1)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _contig1(positions, "positions")
+    _contig1(slot_mapping, "slot_mapping")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, 16, Hkv, d]")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
+    T, hq, d = q.shape
+    nb, bs, hkv, dc = k_cache.shape
+    if k.shape != (T, hkv, d) or v.shape != (T, hkv, d) or dc != d:
+        raise ValueError("k / v / cache shapes disagree with q")
+    if positions.shape[0] != T or slot_mapping.shape[0] != T:
+        raise ValueError("positions / slot_mapping must have num_tokens entries")
+    qs, qh = _rows(q, "q")
+    ks, kh = _rows(k, "k")
+    vs, vh = _rows(v, "v")
+    st = _lib.load().pkv_kv_append(
+        q.data_ptr(), qs, qh, k.data_ptr(), ks, kh, v.data_ptr(), vs, vh,
+        positions.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        T, hq, hkv, d, nb, bs, float(rope_theta), _stream_ptr(stream))
+    _lib.check("pkv_kv_append", st)
+
+
+def workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq):
+    """Bytes of workspace ``paged_attention`` needs (``pkv_paged_attention_workspace_size``)."""
+    n = _lib.load().pkv_paged_attention_workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads,
+                                                       head_dim, max_blocks_per_seq)
+    if n == 0:
+        raise ValueError("invalid sizes for paged_attention")
+    return int(n)
+
+
+def alloc_workspace(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                    device=None):
+    n = workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq)
+    # 256-byte alignment: torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, out=None,
+                    workspace=None, max_blocks_per_seq=None, stream=None):
+    """Paged GQA over a ragged prefill/decode batch (``pkv_paged_attention``).  Returns out."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    _contig1(context_lens, "context_lens")
+    _contig1(query_start_loc, "query_start_loc")
+    if block_tables.stride(1) != 1:
+        raise ValueError("block_tables rows must be contiguous")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, 16, Hkv, d]")
+    T, hq, d = q.shape
+    nb, bs, hkv, dc = k_cache.shape
+    if dc != d or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shapes disagree with q")
+    B = context_lens.shape[0]
+    if query_start_loc.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("query_start_loc must have num_seqs + 1 entries, block_tables num_seqs rows")
+    mb = block_tables.shape[1] if max_blocks_per_seq is None else int(max_blocks_per_seq)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    _need(out, "out", torch.bfloat16, 3)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = alloc_workspace(T, B, hq, hkv, d, mb, device=q.device)
+    qs, qh = _rows(q, "q")
+    os_, oh = _rows(out, "out")
+    st = _lib.load().pkv_paged_attention(
+        q.data_ptr(), qs, qh, k_cache.data_ptr(), v_cache.data_ptr(), nb, bs,
+        block_tables.data_ptr(), block_tables.stride(0), mb, context_lens.data_ptr(),
+        query_start_loc.data_ptr(), B, out.data_ptr(), os_, oh, T, hq, hkv, d, float(scale),
+        workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    _lib.check("pkv_paged_attention", st)
+    return out
+
+
+def set_decode_ctas(n):
+    """Override the decode split-K grid (0 = one CTA per SM).  Process-wide."""
+    _lib.check("pkv_set_decode_ctas", _lib.load().pkv_set_decode_ctas(int(n)))
+
+
+def get_device_error(clear=True, stream=None):
+    """Synchronise the stream and return the or-ed PKV_DEVERR_* bits of the current device."""
+    bits = ctypes.c_uint32(0)
+    st = _lib.load().pkv_get_device_error(ctypes.byref(bits), 1 if clear else 0, _stream_ptr(stream))
+    _lib.check("pkv_get_device_error", st)
+    return int(bits.value)
+
+
+def set_kernel_events(kernel, start=None, stop=None):
+    """Record torch.cuda.Event ``start``/``stop`` around every launch of ``kernel``
+    ("kv_append", "plan", "prefill", "decode", "merge"); None switches it off."""
+    which = _lib.KERNELS[kernel]
+    sp = ctypes.c_void_p(start.cuda_event) if start is not None else None
+    ep = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
+    _lib.check("pkv_set_kernel_events", _lib.load().pkv_set_kernel_events(which, sp, ep))

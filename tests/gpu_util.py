@@ -1,0 +1,80 @@
+"""Helpers for the GPU tests: upload seeded batches, run the CUDA path, compare with the oracle."""
+
+import functools
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_gqa_14_gb300 import ops
+from paged_kv_gqa_14_gb300 import workloads as W
+
+MAX_ABS = 2e-2  # attention tolerance vs the fp64 oracle (bf16 in, fp32 accumulate)
+MEAN_ABS = 2e-3
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def bf16_to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev())
+
+
+def dev_to_bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def idx_to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+
+
+class Dev:
+    """A batch resident on the GPU."""
+
+    def __init__(self, bt, q=None, k_cache=None, v_cache=None):
+        self.bt = bt
+        self.q = bf16_to_dev(bt.q if q is None else q)
+        self.k = bf16_to_dev(bt.k)
+        self.v = bf16_to_dev(bt.v)
+        self.k_cache = bf16_to_dev(bt.k_cache if k_cache is None else k_cache)
+        self.v_cache = bf16_to_dev(bt.v_cache if v_cache is None else v_cache)
+        self.positions = idx_to_dev(bt.positions)
+        self.slots = idx_to_dev(bt.slot_mapping)
+        self.block_tables = idx_to_dev(bt.block_tables)
+        self.context_lens = idx_to_dev(bt.context_lens)
+        self.qsl = idx_to_dev(bt.query_start_loc)
+
+    def append(self):
+        ops.kv_append(self.q, self.k, self.v, self.positions, self.slots, self.k_cache, self.v_cache,
+                      self.bt.rope_theta)
+
+    def attend(self, out=None):
+        return ops.paged_attention(self.q, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+                                   self.qsl, self.bt.scale, out=out)
+
+
+@functools.lru_cache(maxsize=2)
+def config_with_oracle(index):
+    """(batch, q_rot, k_cache, v_cache, oracle out) for a workload, computed once per process."""
+    bt = W.config(index)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc,
+                                 bt.scale)
+    return bt, q_rot, kc, vc, ref
+
+
+def assert_close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (
+        f"{what}: max abs {err.max():.3e} (<= {MAX_ABS}), mean abs {err.mean():.3e} (<= {MEAN_ABS})")
+    return err.max(), err.mean()
+
+
+def ulp_bf16(x):
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(np.maximum(x, 2.0**-126))
+    return np.ldexp(1.0, e - 8)

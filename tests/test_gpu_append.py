@@ -1,0 +1,105 @@
+"""kv_append on the GPU against the fp64 oracle: bit-exact slot placement and V copy,
+untouched rows bit-unchanged (NaN poison included), rotated K and q within 1 bf16 ulp."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_gqa_14_gb300 import ops
+from paged_kv_gqa_14_gb300 import workloads as W
+from tests.gpu_util import Dev, bf16_to_dev, dev_to_bits, idx_to_dev, ulp_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_append(bt, d):
+    d.append()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    gk = dev_to_bits(d.k_cache)
+    gv = dev_to_bits(d.v_cache)
+    # V: every row bit-identical (written rows are copies, the rest untouched)
+    assert np.array_equal(gv, vc)
+    # K: untouched rows bit-identical; written rows within one bf16 ulp of the fp64 rotation
+    written = np.zeros(bt.k_cache.shape[:2], dtype=bool)
+    for s in bt.slot_mapping:
+        if s >= 0:
+            written[s // 16, s % 16] = True
+    assert np.array_equal(gk[~written], kc[~written])
+    kref = oracle.bf16_bits_to_f64(kc[written])
+    kgot = oracle.bf16_bits_to_f64(gk[written])
+    assert np.all(np.abs(kgot - kref) <= ulp_bf16(kref))
+    qgot = oracle.bf16_bits_to_f64(dev_to_bits(d.q))
+    qref = oracle.bf16_bits_to_f64(q_rot)
+    assert np.all(np.abs(qgot - qref) <= ulp_bf16(qref))
+    return (kgot != kref).mean()
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_append_matches_oracle_on_workloads(index):
+    bt = W.config(index)
+    frac_off = _check_append(bt, Dev(bt))
+    assert frac_off < 0.01  # 1-ulp differences are rare rounding ties, not a pattern
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_append_random_shapes(seed):
+    bt = W.random_case(seed, head_dims=(64, 128), groups=(1, 2, 3, 7), kv_heads=(1, 2, 4, 8))
+    _check_append(bt, Dev(bt))
+
+
+def test_append_skips_negative_slots_and_flags_out_of_range():
+    bt = W.make_batch([5, 20, 33, 2], [1, 1, 1, 1], 8, 4, 128, 12, seed=3)
+    slots = bt.slot_mapping.copy()
+    slots[1] = -1  # padding token
+    slots[2] = 12 * 16 + 5  # past the pool: must be skipped and flagged
+    d = Dev(bt)
+    d.slots = idx_to_dev(slots)
+    ops.get_device_error()  # clear
+    d.append()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0x1
+    gk, gv = dev_to_bits(d.k_cache), dev_to_bits(d.v_cache)
+    for t in (1, 2):
+        b, o = divmod(int(bt.slot_mapping[t]), 16)
+        assert np.array_equal(gk[b, o], bt.k_cache[b, o])
+        assert np.array_equal(gv[b, o], bt.v_cache[b, o])
+    for t in (0, 3):
+        b, o = divmod(int(slots[t]), 16)
+        assert np.array_equal(gv[b, o], bt.v[t])
+
+
+def test_append_position_zero_is_exact_copy():
+    bt = W.make_batch([1, 1], [1, 1], 4, 2, 64, 4, seed=9)
+    d = Dev(bt)
+    d.append()
+    gk = dev_to_bits(d.k_cache)
+    for t in range(2):
+        b, o = divmod(int(bt.slot_mapping[t]), 16)
+        assert np.array_equal(gk[b, o], bt.k[t])
+    assert np.array_equal(dev_to_bits(d.q), bt.q)
+
+
+def test_append_reads_strided_views_of_a_packed_qkv_buffer():
+    bt = W.make_batch([17, 40, 3], [1, 1, 1], 16, 8, 128, 10, seed=4)
+    T, hq, hkv, dd = bt.num_tokens, 16, 8, 128
+    packed = np.zeros((T, (hq + 2 * hkv) * dd), dtype=np.uint16)
+    packed[:, : hq * dd] = bt.q.reshape(T, -1)
+    packed[:, hq * dd : (hq + hkv) * dd] = bt.k.reshape(T, -1)
+    packed[:, (hq + hkv) * dd :] = bt.v.reshape(T, -1)
+    P = bf16_to_dev(packed)
+    q = P[:, : hq * dd].view(T, hq, dd)
+    k = P[:, hq * dd : (hq + hkv) * dd].view(T, hkv, dd)
+    v = P[:, (hq + hkv) * dd :].view(T, hkv, dd)
+    d = Dev(bt)
+    ops.kv_append(q, k, v, d.positions, d.slots, d.k_cache, d.v_cache, bt.rope_theta)
+    ref = Dev(bt)
+    ref.append()
+    assert torch.equal(d.k_cache.view(torch.int16), ref.k_cache.view(torch.int16))
+    assert torch.equal(d.v_cache.view(torch.int16), ref.v_cache.view(torch.int16))
+    assert torch.equal(q.contiguous().view(torch.int16), ref.q.view(torch.int16))
+    # k and v inside the packed buffer are untouched
+    assert np.array_equal(dev_to_bits(P)[:, hq * dd :], packed[:, hq * dd :])

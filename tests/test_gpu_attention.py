@@ -1,0 +1,169 @@
+"""paged_attention on the GPU against the fp64 oracle (max abs <= 2e-2, mean abs <= 2e-3),
+on all five workloads at full size, random mixed micro-batches over every supported
+shape, and the properties that hold at any size."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_gqa_14_gb300 import ops
+from paged_kv_gqa_14_gb300 import workloads as W
+from tests.gpu_util import (Dev, assert_close, bf16_to_dev, config_with_oracle, dev_to_bits, idx_to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _attend_oracle_inputs(bt, q_rot, kc, vc):
+    d = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
+    out = d.attend()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    return out.float().cpu().numpy(), d
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_attention_matches_oracle_on_workloads(index):
+    bt, q_rot, kc, vc, ref = config_with_oracle(index)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert_close(got, ref, bt.name)
+
+
+@pytest.mark.parametrize("index", [1, 3, 5])
+def test_full_step_append_then_attention(index):
+    bt, q_rot, kc, vc, ref = config_with_oracle(index)
+    d = Dev(bt)
+    d.append()
+    out = d.attend()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    assert_close(out.float().cpu().numpy(), ref, bt.name + " (append + attention)")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_mixed_batches(seed):
+    bt = W.random_case(seed, max_seqs=6, max_ctx=300, head_dims=(64, 128), groups=(1, 2, 3, 4, 5, 6, 7, 8),
+                       kv_heads=(1, 2, 4, 8))
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert_close(got, ref, bt.name)
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 600])
+def test_split_count_does_not_change_the_result(ctas):
+    bt, q_rot, kc, vc, ref = config_with_oracle(3)
+    auto, d = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    try:
+        ops.set_decode_ctas(ctas)
+        forced = d.attend().float().cpu().numpy()
+    finally:
+        ops.set_decode_ctas(0)
+    assert_close(forced, ref, f"decode ctas={ctas}")
+    assert np.abs(forced - auto).max() <= 2e-2
+
+
+def test_physical_block_permutation_is_bit_identical():
+    bt, q_rot, kc, vc, _ = config_with_oracle(2)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    perm = np.random.default_rng(0).permutation(bt.num_blocks)
+    kc2 = np.empty_like(kc)
+    vc2 = np.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt2 = W.Batch(**{**bt.__dict__})
+    bt2.block_tables = np.where(bt.block_tables >= 0, perm[np.maximum(bt.block_tables, 0)], -1).astype(np.int32)
+    got2, _ = _attend_oracle_inputs(bt2, q_rot, kc2, vc2)
+    assert np.array_equal(got, got2)
+
+
+def test_single_key_context_returns_v_exactly():
+    bt, q_rot, kc, vc, _ = config_with_oracle(1)  # sequence 0 has context 1
+    _, d = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    out = dev_to_bits(d.attend())
+    G = bt.num_q_heads // bt.num_kv_heads
+    for h in range(bt.num_q_heads):
+        assert np.array_equal(out[0, h], bt.v[0, h // G])
+
+
+def test_last_prefill_row_equals_decode_at_same_context():
+    # a 40-row chunk over 100 earlier tokens vs a one-row decode of its last token
+    bt = W.make_batch([140], [40], 16, 8, 128, 12, seed=31)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    pf, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    bt_dec = W.Batch(**{**bt.__dict__})
+    bt_dec.query_start_loc = np.array([0, 1], dtype=np.int32)
+    dec, _ = _attend_oracle_inputs(bt_dec, q_rot[-1:], kc, vc)
+    assert np.abs(pf[-1] - dec[0]).max() <= 2e-2
+
+
+def test_empty_spans_and_uncovered_rows_are_untouched():
+    bt = W.make_batch([30, 50, 20, 70], [1, 0, 5, 1], 8, 2, 64, 16, seed=32)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    # one extra trailing row that no span covers
+    q_ext = np.concatenate([q_rot, q_rot[:1]])
+    d = Dev(bt, q=q_ext, k_cache=kc, v_cache=vc)
+    sentinel = torch.full((bt.num_tokens + 1, 8, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    d.attend(out=sentinel)
+    torch.cuda.synchronize()
+    got = sentinel.float().cpu().numpy()
+    assert_close(got[:-1], ref, "empty spans")
+    assert np.all(got[-1] == 7.0)
+
+
+def test_attention_on_strided_q_and_out():
+    bt, q_rot, kc, vc, ref = config_with_oracle(1)
+    T, hq, d = q_rot.shape
+    wide = np.zeros((T, hq + 3, d), dtype=np.uint16)
+    wide[:, 1 : hq + 1] = q_rot
+    dd = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
+    qw = bf16_to_dev(wide)[:, 1 : hq + 1]
+    outw = torch.zeros((T, hq + 2, d), dtype=torch.bfloat16, device="cuda")
+    ops.paged_attention(qw, dd.k_cache, dd.v_cache, dd.block_tables, dd.context_lens, dd.qsl, bt.scale,
+                        out=outw[:, 2:])
+    assert_close(outw[:, 2:].float().cpu().numpy(), ref, "strided")
+    assert torch.all(outw[:, :2] == 0)
+
+
+def test_device_errors_are_flagged_not_faulted():
+    bt = W.make_batch([30, 50, 20], [1, 1, 1], 8, 4, 128, 10, seed=33)
+    d = Dev(bt)
+    d.append()
+    ops.get_device_error()  # clear
+    bad = bt.block_tables.copy()
+    bad[1, 1] = 10_000  # outside the pool: read redirected, bit set
+    d.block_tables = idx_to_dev(bad)
+    d.attend()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() & 0x2
+    d.block_tables = idx_to_dev(bt.block_tables)
+    ctx = bt.context_lens.copy()
+    ctx[2] = bt.block_tables.shape[1] * 16 + 1  # longer than its block-table row
+    d.context_lens = idx_to_dev(ctx)
+    d.attend()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() & 0x8
+    d.context_lens = idx_to_dev(bt.context_lens)
+    qsl = bt.query_start_loc.copy()
+    qsl[2] = qsl[1] - 1 if qsl[1] > 0 else 0  # non-monotone
+    qsl[1] = qsl[1] + 1
+    d.qsl = idx_to_dev(qsl.astype(np.int32))
+    d.attend()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() & 0x4
+    # the context is still usable
+    d.qsl = idx_to_dev(bt.query_start_loc)
+    d.attend()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+
+
+def test_nan_poisoned_slots_never_leak():
+    # every workload is generated with NaN in all unreferenced slots; full-size outputs are finite
+    bt, q_rot, kc, vc, _ = config_with_oracle(5)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert np.all(np.isfinite(got))
