@@ -218,6 +218,8 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     bt = W.config(args.workload, poison=False)
+    if args.seqs:
+        bt = sub_batch(bt, range(min(args.seqs, bt.num_seqs)))
     kv_u = kv_unique_bytes(bt)
     kv_l = kv_logical_bytes(bt)
     algo = decode_algorithmic_bytes(bt, kv_u)
@@ -454,6 +456,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--seqs", type=int, default=0, help="only the first N sequences (small profiling case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args()

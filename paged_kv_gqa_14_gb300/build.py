@@ -21,8 +21,9 @@ LIB = os.path.join(BUILD, "libpkv.so")
 
 SOURCES = ["abi.cu", "kv_append.cu", "attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-         "--use_fast_math"]
+# No --use_fast_math: sincosf in the RoPE kernel stays the accurate library routine; the
+# kernels call fast approximations (ex2.approx) explicitly where they want them.
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 
 
 def nvcc():

@@ -150,6 +150,9 @@ def set_kernel_events(kernel, start=None, stop=None):
     """Record torch.cuda.Event ``start``/``stop`` around every launch of ``kernel``
     ("kv_append", "plan", "prefill", "decode", "merge"); None switches it off."""
     which = _lib.KERNELS[kernel]
+    for e in (start, stop):
+        if e is not None and e.cuda_event == 0:
+            e.record()  # torch creates the CUDA event lazily, on its first record
     sp = ctypes.c_void_p(start.cuda_event) if start is not None else None
     ep = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
     _lib.check("pkv_set_kernel_events", _lib.load().pkv_set_kernel_events(which, sp, ep))

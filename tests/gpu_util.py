@@ -78,3 +78,23 @@ def ulp_bf16(x):
     x = np.abs(np.asarray(x, dtype=np.float64))
     _, e = np.frexp(np.maximum(x, 2.0**-126))
     return np.ldexp(1.0, e - 8)
+
+
+def rope_tol(x_bits, ref):
+    """Allowed |gpu - oracle| for a rotated bf16 value.
+
+    The kernel rotates in fp32 (x cos a - y sin a with sincosf, a few fp32 roundings, error
+    well below 2^-21 (|x| + |y|)) and rounds once to bf16.  Where the result is not tiny that
+    moves the bf16 value by at most one ulp (only near rounding ties); where x cos a and
+    y sin a cancel, the fp32 absolute error can exceed an ulp of the tiny result.  Bound:
+    one bf16 ulp of the reference plus 2^-21 times the pair's magnitude |x_i| + |x_{i+d/2}|.
+    """
+    x = np.abs(np.asarray(x_bits_to_f64(x_bits)))
+    half = x.shape[-1] // 2
+    m = x[..., :half] + x[..., half:]
+    pair = np.concatenate([m, m], axis=-1)
+    return ulp_bf16(ref) + 2.0**-21 * pair
+
+
+def x_bits_to_f64(bits):
+    return oracle.bf16_bits_to_f64(bits)
