@@ -294,6 +294,23 @@ def run_gpu(args, rank, world, local_rank):
     achieved = algo / (dec_avg * 1e-3) / 1e9
     traffic = decode_traffic(bt.name, algo)
 
+    # the same step captured once in a CUDA graph and replayed (host launch cost removed)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    g0, g1 = ev(), ev()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(K):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1) / K
+    del graph
+
     # end to end through the public API with host buffers: pinned inputs -> device, step,
     # result -> pinned host, every step
     host_in = {
@@ -381,6 +398,11 @@ def run_gpu(args, rank, world, local_rank):
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
             "algorithmic_bytes": algo,
+        },
+        "graph": {
+            "ms_per_step": round(graph_ms, 5),
+            "value": round(world * kv_u / (graph_ms * 1e-3) / 1e9, 2),
+            "tokens_per_s_per_layer": round(world * bt.num_tokens / (graph_ms * 1e-3), 1),
         },
         "e2e": {
             "value": round(world * kv_u / (e2e_ms * 1e-3) / 1e9, 2),

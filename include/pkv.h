@@ -172,6 +172,16 @@ PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64
 PKV_API int pkv_set_decode_ctas(int32_t ctas);
 
 /*
+ * pkv_set_decode_kernel -- choose the arithmetic of the decode split-K kernel for later calls:
+ * 0 automatic (tensor cores when num_q_heads / num_kv_heads >= 3, else CUDA cores),
+ * 1 CUDA cores (per-lane fp32 FMA, warp-shuffle reductions),
+ * 2 tensor cores (bf16 mma.sync with the GQA group as the N dimension).
+ * Both compute the same result up to fp32 rounding.  Process-wide; for tests and tuning.
+ * Returns PKV_ERR_SHAPE for another value.
+ */
+PKV_API int pkv_set_decode_kernel(int kind);
+
+/*
  * pkv_set_kernel_events -- instrumentation: from now on, every launch of kernel `which`
  * records `start_event` on its stream just before the launch and `stop_event` just after
  * (both cudaEvent_t passed as void*, created by the caller).  NULL events (or which = 0)

@@ -31,6 +31,7 @@ SIGNATURES = {
          _c_p],
     ),
     "pkv_set_decode_ctas": (ctypes.c_int, [ctypes.c_int32]),
+    "pkv_set_decode_kernel": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_kernel_events": (ctypes.c_int, [ctypes.c_int, _c_p, _c_p]),
     "pkv_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _c_p]),
 }

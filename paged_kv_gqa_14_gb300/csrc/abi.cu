@@ -19,6 +19,7 @@ std::once_flag g_dev_once[kMaxDevices];
 unsigned int* g_err_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 std::atomic<int> g_decode_ctas_override{0};
+std::atomic<int> g_decode_kernel{0};
 constexpr int kNumKernels = 6;
 std::atomic<void*> g_events[kNumKernels][2];
 
@@ -64,6 +65,8 @@ void record_kernel_event(int which, bool after, cudaStream_t stream) {
   if (e) cudaEventRecord(static_cast<cudaEvent_t>(e), stream);
 }
 
+int decode_kernel_choice() { return g_decode_kernel.load(); }
+
 int decode_ctas_for_device() {
   const int o = g_decode_ctas_override.load();
   if (o > 0) return o;
@@ -95,6 +98,12 @@ int pkv_version(void) { return 100; }
 int pkv_set_decode_ctas(int32_t ctas) {
   if (ctas < 0) return PKV_ERR_SHAPE;
   g_decode_ctas_override.store(ctas);
+  return PKV_OK;
+}
+
+int pkv_set_decode_kernel(int kind) {
+  if (kind < 0 || kind > 2) return PKV_ERR_SHAPE;
+  g_decode_kernel.store(kind);
   return PKV_OK;
 }
 
@@ -217,6 +226,7 @@ int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k
   a.head_dim = static_cast<int>(head_dim);
   a.scale = scale;
   a.decode_ctas = ctas;
+  a.decode_kernel = decode_kernel_choice();
   a.plan = plan_view(workspace, ps);
   a.max_tiles = ps.max_tiles;
   a.err = g_err_ptr[dev];

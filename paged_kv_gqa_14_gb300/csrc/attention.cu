@@ -7,7 +7,10 @@
 //   2. prefill kernel   (persistent) causal varlen tiles for spans longer than one row
 //   3. decode kernel    (1 CTA/SM) split-K over page groups for spans of one row
 //   4. merge_kernel     (B CTAs)  combine the split states of sequences cut by a CTA boundary
+#include <mutex>
+
 #include "decode.cuh"
+#include "decode_tc.cuh"
 #include "prefill.cuh"
 
 namespace pkv {
@@ -243,17 +246,99 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// cuTensorMapEncodeTiled, fetched from the driver once (no link-time dependency on libcuda)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// The pool [num_blocks][16][Hkv][d] as a 4-D tensor {d, Hkv, 16, num_blocks}; a box is the
+// 16 token rows x 64 dims of one kv head in one block, 128-byte swizzled.
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv), 16,
+                              static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hkv) * D * 2,
+                                 static_cast<cuuint64_t>(16) * hkv * D * 2};
+  const cuuint32_t box[4] = {64, 1, 16, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
+  using C = DecodeTcCfg<D, G>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  DecodeTcParams P;
+  if (!make_pool_map(&P.tmap_k, a.k_cache, a.num_blocks, a.hkv, D) ||
+      !make_pool_map(&P.tmap_v, a.v_cache, a.num_blocks, a.hkv, D))
+    return cudaErrorInvalidValue;
+  DecodeParams& p = P.p;
+  p.q = static_cast<const bf16*>(a.q);
+  p.q_st = a.q_st;
+  p.q_sh = a.q_sh;
+  p.k_cache = static_cast<const bf16*>(a.k_cache);
+  p.v_cache = static_cast<const bf16*>(a.v_cache);
+  p.num_blocks = a.num_blocks;
+  p.block_tables = a.block_tables;
+  p.bt_stride = a.bt_stride;
+  p.context_lens = a.context_lens;
+  p.qsl = a.qsl;
+  p.out = static_cast<bf16*>(a.out);
+  p.o_st = a.o_st;
+  p.o_sh = a.o_sh;
+  p.hkv = a.hkv;
+  p.hq = a.hq;
+  p.qscale = a.scale * 1.4426950408889634f;
+  p.plan = a.plan;
+  p.err = a.err;
+  record_kernel_event(PKV_KERNEL_DECODE, false, stream);
+  decode_tc_kernel<D, G><<<a.decode_ctas, (kDecodeWarps + 1) * 32, C::kSmemBytes, stream>>>(P);
+  record_kernel_event(PKV_KERNEL_DECODE, true, stream);
+  return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_decode_pick(const AttnArgs& a, cudaStream_t stream) {
+  const int kind = a.decode_kernel != 0 ? a.decode_kernel : (G >= kTensorDecodeMinGroup ? 2 : 1);
+  return kind == 2 ? launch_decode_tc<D, G>(a, stream) : launch_decode<D, G>(a, stream);
+}
+
 template <int D>
 cudaError_t launch_decode_g(const AttnArgs& a, cudaStream_t stream) {
   switch (a.hq / a.hkv) {
-    case 1: return launch_decode<D, 1>(a, stream);
-    case 2: return launch_decode<D, 2>(a, stream);
-    case 3: return launch_decode<D, 3>(a, stream);
-    case 4: return launch_decode<D, 4>(a, stream);
-    case 5: return launch_decode<D, 5>(a, stream);
-    case 6: return launch_decode<D, 6>(a, stream);
-    case 7: return launch_decode<D, 7>(a, stream);
-    case 8: return launch_decode<D, 8>(a, stream);
+    case 1: return launch_decode_pick<D, 1>(a, stream);
+    case 2: return launch_decode_pick<D, 2>(a, stream);
+    case 3: return launch_decode_pick<D, 3>(a, stream);
+    case 4: return launch_decode_pick<D, 4>(a, stream);
+    case 5: return launch_decode_pick<D, 5>(a, stream);
+    case 6: return launch_decode_pick<D, 6>(a, stream);
+    case 7: return launch_decode_pick<D, 7>(a, stream);
+    case 8: return launch_decode_pick<D, 8>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,0 +1,374 @@
+// Decode split-K on the tensor cores: the GQA group is the contraction's N dimension.
+//
+// Same work decomposition, producer/consumer ring and split states as the CUDA-core
+// decode kernel (decode.cuh): a unit is P = 8 / Hkv pages of one decode sequence with all kv
+// heads, consumer warp w owns page w / Hkv and kv head w % Hkv, and every K/V page is read
+// from HBM once per GQA group.  What changes is the arithmetic of a (page, kv head):
+//
+//   S^T [16 tokens x 8] = K_page [16 x d] . Q_g^T [d x 8]       mma.sync m16n8k16, bf16 -> fp32
+//   online softmax over the 16 token rows of each head column (warp shuffles)
+//   P^T packed to bf16 and transposed in registers with movmatrix
+//   O^T [d x 8]        += V_page^T [d x 16] . P^T [16 x 8]       mma.sync m16n8k16
+//
+// M = the page's 16 tokens, N = 8 >= G query heads (unused columns are zero q), K = d for
+// QK^T and 16 tokens for PV.  This removes the G-proportional CUDA-core work (G FMAs per
+// loaded element plus shuffle reductions) that caps the scalar kernel at large G.
+//
+// K/V pages are staged by 4-D TMA tensor loads (tensor map over the pool viewed as
+// [num_blocks][16][Hkv][d]) in boxes of 16 tokens x 64 dims of one kv head with the 128-byte
+// swizzle, so the ldmatrix reads of 8 token rows hit 8 different bank groups.
+#pragma once
+
+#include <cuda.h>
+
+#include "decode.cuh"
+
+namespace pkv {
+
+struct DecodeTcParams {
+  CUtensorMap tmap_k;  // 4-D: {d, Hkv, 16, num_blocks}, box {64, 1, 16, 1}, 128B swizzle
+  CUtensorMap tmap_v;
+  DecodeParams p;
+};
+
+template <int D, int G>
+struct DecodeTcCfg {
+  static constexpr int HALVES = D / 64;                 // 64-dim boxes per head row
+  static constexpr int kBoxBytes = 16 * 64 * 2;         // one box: 16 tokens x 64 dims
+  static constexpr int kPartBytes = kDecodeWarps * HALVES * kBoxBytes;  // K (or V) of a stage
+  static constexpr int kStageBytes = 2 * kPartBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kXbufBytes = kDecodeWarps * G * (D + 2) * 4;
+  static constexpr int kReserve = kBarBytes + kXbufBytes + 1024;  // + alignment slack
+  static constexpr int kSmemLimit = 227 * 1024;
+  static constexpr int kStagesFit = (kSmemLimit - kReserve) / kStageBytes;
+  static constexpr int STAGES = kStagesFit > 4 ? 4 : kStagesFit;
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kReserve;
+  static_assert(STAGES >= 2, "decode pipeline needs at least two stages");
+  static_assert(G >= 1 && G <= 8, "the GQA group is the mma N dimension (8)");
+};
+
+__device__ __forceinline__ void tma_load_4d(void* dst_smem, const CUtensorMap* map, int c0, int c1, int c2,
+                                            int c3, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_tc(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t_tc(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// byte offset of 16-byte chunk `c` (0..7) of token row `t` inside a 128B-swizzled box
+__device__ __forceinline__ uint32_t box_off(int t, int c) { return t * 128 + ((c ^ (t & 7)) << 4); }
+
+template <int D, int G>
+__global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
+    decode_tc_kernel(const __grid_constant__ DecodeTcParams P) {
+  using C = DecodeTcCfg<D, G>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int HALVES = C::HALVES;
+  constexpr int KS = D / 16;  // k-steps of QK^T, m-tiles of PV
+  const DecodeParams& p = P.p;
+  extern __shared__ unsigned char smem_raw[];
+  // 1024-byte alignment for the 128B swizzle pattern
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+  uint64_t* empty = full + STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
+  int* seg0 = const_cast<int*>(abort_flag + 1);
+  float* xbuf = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes + C::kBarBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int* hdr = p.plan.header;
+  const int n_dec = hdr[0];
+  const int U = hdr[1];
+  const int W = hdr[2];
+  const int ubeg = blockIdx.x * W;
+  const int uend = min(U, ubeg + W);
+  if (ubeg >= uend) return;
+
+  const int* dec_unit = p.plan.dec_unit;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecodeWarps);
+    }
+    fence_mbar_init();
+    *abort_flag = 0;
+    int lo = 0, hi = n_dec - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (dec_unit[mid] <= ubeg) lo = mid; else hi = mid - 1;
+    }
+    *seg0 = lo;
+  }
+  __syncthreads();
+  const int i_first = *seg0;
+  const int hkv = p.hkv;
+  const int pps = kDecodeWarps / hkv;
+  const uint32_t page_bytes = static_cast<uint32_t>(hkv * HALVES * C::kBoxBytes);
+
+  if (warp == kDecodeWarps) {
+    // ------------------------------------------------------------------ producer warp
+    const uint64_t pol = l2_policy_evict_first();
+    // lane -> (K or V, page, kv head, half) of the unit's boxes; 16*HALVES boxes <= 32
+    const int per_kv = kDecodeWarps * HALVES;
+    const int kv = lane / per_kv;
+    const int rem = lane - kv * per_kv;
+    const int bp = rem / (hkv * HALVES);
+    const int rem2 = rem - bp * hkv * HALVES;
+    const int bh = rem2 / HALVES;
+    const int bhalf = rem2 - bh * HALVES;
+    const bool lane_has_box = lane < 2 * per_kv;
+    int i = i_first;
+    int ustart = dec_unit[i], unext = dec_unit[i + 1];
+    int b = p.plan.dec_seq[i];
+    int npages = ceil_div(p.context_lens[b], 16);
+    int it = 0;
+    for (int u = ubeg; u < uend; ++u, ++it) {
+      while (u >= unext) {
+        ++i;
+        ustart = unext;
+        unext = dec_unit[i + 1];
+        b = p.plan.dec_seq[i];
+        npages = ceil_div(p.context_lens[b], 16);
+      }
+      const int pg0 = (u - ustart) * pps;
+      const int npg = min(pps, npages - pg0);
+      const int s = it % STAGES;
+      if (it >= STAGES && !wait_or_abort(&empty[s], ((it / STAGES) - 1) & 1, p.err, abort_flag)) break;
+      int blk = 0;
+      const bool issue = lane_has_box && bp < npg;
+      if (issue) {
+        blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + pg0 + bp];
+        if (blk < 0 || blk >= p.num_blocks) {
+          raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+          blk = 0;
+        }
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * npg * page_bytes);
+      __syncwarp();
+      if (issue) {
+        unsigned char* dst = stages + s * C::kStageBytes + kv * C::kPartBytes +
+                             ((bp * hkv + bh) * HALVES + bhalf) * C::kBoxBytes;
+        tma_load_4d(dst, kv ? &P.tmap_v : &P.tmap_k, bhalf * 64, bh, 0, blk, &full[s], pol);
+      }
+    }
+    const int issued = it;
+    for (int k = max(0, issued - STAGES); k < issued; ++k)
+      wait_or_abort(&full[k % STAGES], (k / STAGES) & 1, p.err, abort_flag);
+    return;
+  }
+
+  // -------------------------------------------------------------------- consumer warps
+  const int pw = warp / hkv;
+  const int h = warp - pw * hkv;
+  const int gr = lane >> 2, tig = lane & 3;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+
+  uint32_t qb[KS][2];  // Q^T B fragments: head gr (zero past G), dims of k-step kk
+  float acc[KS][4];    // O^T: dims 16mt + gr (+8), heads 2tig (+1)
+  float mrun[2], lrun[2];
+  int i = i_first;
+  int ustart = 0, unext = 0, b = 0, ctx = 0, npages = 0;
+  int64_t tq = 0;
+  bool seg_start = true;
+  bool ok = true;
+  int it = 0;
+  const uint32_t stage_base = smem_u32(stages);
+  for (int u = ubeg; u < uend; ++u, ++it) {
+    if (seg_start) {
+      ustart = dec_unit[i];
+      unext = dec_unit[i + 1];
+      b = p.plan.dec_seq[i];
+      ctx = p.context_lens[b];
+      npages = ceil_div(ctx, 16);
+      tq = p.qsl[b];
+      const bool hv = gr < G;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          p.q + tq * p.q_st + static_cast<int64_t>(h * G + (hv ? gr : 0)) * p.q_sh);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qb[kk][0] = hv ? qrow[kk * 8 + tig] : 0u;
+        qb[kk][1] = hv ? qrow[kk * 8 + 4 + tig] : 0u;
+      }
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+      mrun[0] = mrun[1] = NEG_INF;
+      lrun[0] = lrun[1] = 0.f;
+      seg_start = false;
+    }
+    const int s = it % STAGES;
+    if (ok) ok = wait_or_abort(&full[s], (it / STAGES) & 1, p.err, abort_flag);
+    const int pg = (u - ustart) * pps + pw;
+    if (ok && pg < npages) {
+      const int rows = min(16, ctx - pg * 16);
+      const uint32_t kbox = stage_base + s * C::kStageBytes + (pw * hkv + h) * HALVES * C::kBoxBytes;
+      const uint32_t vbox = kbox + C::kPartBytes;
+      if (rows < 16) {
+        // keys past the context: zero their V rows so 0 * (unused slot) cannot poison P.V
+        unsigned char* vgen = stages + s * C::kStageBytes + C::kPartBytes + (pw * hkv + h) * HALVES * C::kBoxBytes;
+        for (int idx = lane; idx < (16 - rows) * 8 * HALVES; idx += 32) {
+          const int hh = idx / ((16 - rows) * 8);
+          const int r2 = idx - hh * (16 - rows) * 8;
+          const int t = rows + (r2 >> 3);
+          *reinterpret_cast<uint4*>(vgen + hh * C::kBoxBytes + t * 128 + ((r2 & 7) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // S^T = K . Q^T
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t a[4];
+          ldsm_x4_tc(a, kbox + (kk >> 2) * C::kBoxBytes + box_off(r, 2 * (kk & 3) + csel));
+          mma_16816(sc, a, qb[kk][0], qb[kk][1]);
+        }
+      }
+      // scale, mask, online softmax over the token rows of each head column
+      const bool v0 = gr < rows, v1 = gr + 8 < rows;
+      sc[0] = v0 ? sc[0] * p.qscale : NEG_INF;
+      sc[1] = v0 ? sc[1] * p.qscale : NEG_INF;
+      sc[2] = v1 ? sc[2] * p.qscale : NEG_INF;
+      sc[3] = v1 ? sc[3] * p.qscale : NEG_INF;
+      float pm0 = fmaxf(sc[0], sc[2]), pm1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        pm0 = fmaxf(pm0, __shfl_xor_sync(0xffffffffu, pm0, off));
+        pm1 = fmaxf(pm1, __shfl_xor_sync(0xffffffffu, pm1, off));
+      }
+      const float mn0 = fmaxf(mrun[0], pm0), mn1 = fmaxf(mrun[1], pm1);
+      const float c0 = fast_exp2(mrun[0] - mn0), c1 = fast_exp2(mrun[1] - mn1);
+      mrun[0] = mn0;
+      mrun[1] = mn1;
+      sc[0] = fast_exp2(sc[0] - mn0);
+      sc[1] = fast_exp2(sc[1] - mn1);
+      sc[2] = fast_exp2(sc[2] - mn0);
+      sc[3] = fast_exp2(sc[3] - mn1);
+      lrun[0] = lrun[0] * c0 + sc[0] + sc[2];
+      lrun[1] = lrun[1] * c1 + sc[1] + sc[3];
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        acc[mt][0] *= c0;
+        acc[mt][1] *= c1;
+        acc[mt][2] *= c0;
+        acc[mt][3] *= c1;
+      }
+      // P^T (tokens x heads) -> B fragments (k = token, n = head) by an 8x8 transpose
+      const uint32_t pb0 = movmatrix_t(pack_bf16x2(sc[0], sc[1]));
+      const uint32_t pb1 = movmatrix_t(pack_bf16x2(sc[2], sc[3]));
+      // O^T += V^T . P^T
+      {
+        const int r = (lane & 7) + 8 * (lane >> 4);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_t_tc(a, vbox + (mt >> 2) * C::kBoxBytes + box_off(r, 2 * (mt & 3) + csel));
+          mma_16816(acc[mt], a, pb0, pb1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    const bool seg_end = (u + 1 == unext) || (u + 1 == uend);
+    if (!seg_end) continue;
+
+    // ---------------------------------------------------------------- segment flush
+    float L0 = lrun[0], L1 = lrun[1];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      L0 += __shfl_xor_sync(0xffffffffu, L0, off);
+      L1 += __shfl_xor_sync(0xffffffffu, L1, off);
+    }
+    float* xb = xbuf + warp * G * (D + 2);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int hh = 2 * tig + j;
+      if (hh < G) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          xb[hh * (D + 2) + 16 * mt + gr] = acc[mt][j];
+          xb[hh * (D + 2) + 16 * mt + gr + 8] = acc[mt][2 + j];
+        }
+        if (gr == 0) {
+          xb[hh * (D + 2) + D] = mrun[j];
+          xb[hh * (D + 2) + D + 1] = j ? L1 : L0;
+        }
+      }
+    }
+    named_bar_sync(1, kDecodeWarps * 32);
+    {
+      const int chunks = p.plan.dec_chunks[i];
+      const int slot = p.plan.dec_slot[i] + (static_cast<int>(blockIdx.x) - ustart / W);
+      const int tid = threadIdx.x;  // 0..255
+      for (int item = tid; item < hkv * G * (D / 4); item += kDecodeWarps * 32) {
+        const int hh = item / (G * (D / 4));
+        const int rem3 = item - hh * G * (D / 4);
+        const int g = rem3 / (D / 4);
+        const int d0 = (rem3 - g * (D / 4)) * 4;
+        float M = NEG_INF;
+        for (int k = 0; k < pps; ++k) M = fmaxf(M, xbuf[((hh + k * hkv) * G + g) * (D + 2) + D]);
+        float num[4] = {0.f, 0.f, 0.f, 0.f};
+        float den = 0.f;
+        for (int k = 0; k < pps; ++k) {
+          const float* e = xbuf + ((hh + k * hkv) * G + g) * (D + 2);
+          const float w = fast_exp2(e[D] - M);  // a warp with no pages: m = -inf -> w = 0
+          den = fmaf(w, e[D + 1], den);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) num[x] = fmaf(w, e[d0 + x], num[x]);
+        }
+        const int hq = hh * G + g;
+        if (chunks == 1) {
+          const float inv = 1.f / den;
+          uint2 o;
+          o.x = pack_bf16x2(num[0] * inv, num[1] * inv);
+          o.y = pack_bf16x2(num[2] * inv, num[3] * inv);
+          *reinterpret_cast<uint2*>(p.out + tq * p.o_st + static_cast<int64_t>(hq) * p.o_sh + d0) = o;
+        } else {
+          const int64_t sh = static_cast<int64_t>(slot) * p.hq + hq;
+          *reinterpret_cast<float4*>(p.plan.part_acc + sh * D + d0) = make_float4(num[0], num[1], num[2], num[3]);
+          if (d0 == 0) *reinterpret_cast<float2*>(p.plan.part_ml + sh * 2) = make_float2(M, den);
+        }
+      }
+    }
+    named_bar_sync(1, kDecodeWarps * 32);
+    seg_start = true;
+    ++i;
+  }
+}
+
+}  // namespace pkv

@@ -11,6 +11,8 @@ constexpr int kBlockSize = 16;       // tokens per KV block (the pool's block_si
 constexpr int kDecodeWarps = 8;      // consumer warps of the decode split-K kernel
 constexpr int kPrefillTileQ = 64;    // query rows per prefill work tile
 constexpr int kMaxHeadDim = 128;
+// GQA group size from which the decode runs on the tensor cores by default
+constexpr int kTensorDecodeMinGroup = 3;
 
 // ---------------------------------------------------------------- work plan layout
 // The planner kernel fills these arrays in the caller's workspace; the decode, prefill
@@ -84,6 +86,7 @@ struct AttnArgs {
   int hq, hkv, head_dim;
   float scale;
   int decode_ctas;
+  int decode_kernel;  // 0 automatic, 1 CUDA-core (warp-shuffle), 2 tensor-core (mma.sync)
   Plan plan;
   int64_t max_tiles;
   unsigned int* err;
@@ -96,5 +99,6 @@ int device_sm_count();
 // (pkv_set_kernel_events); `after` selects the stop event.
 void record_kernel_event(int which, bool after, cudaStream_t stream);
 int decode_ctas_for_device();
+int decode_kernel_choice();
 
 }  // namespace pkv

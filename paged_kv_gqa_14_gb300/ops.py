@@ -138,6 +138,14 @@ def set_decode_ctas(n):
     _lib.check("pkv_set_decode_ctas", _lib.load().pkv_set_decode_ctas(int(n)))
 
 
+DECODE_KERNELS = {"auto": 0, "simt": 1, "tensor": 2}
+
+
+def set_decode_kernel(kind):
+    """Decode arithmetic for later calls: "auto", "simt" (CUDA cores) or "tensor" (mma.sync)."""
+    _lib.check("pkv_set_decode_kernel", _lib.load().pkv_set_decode_kernel(DECODE_KERNELS[kind]))
+
+
 def get_device_error(clear=True, stream=None):
     """Synchronise the stream and return the or-ed PKV_DEVERR_* bits of the current device."""
     bits = ctypes.c_uint32(0)
