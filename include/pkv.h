@@ -164,6 +164,40 @@ PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64
                         void* workspace_dev, size_t workspace_bytes, void* stream);
 
 /*
+ * pkv_paged_attention_noalloc -- pkv_paged_attention for callers that cannot allocate
+ * device memory.  It has no counterpart in the pages; it is a deployment convenience.
+ *
+ * Some callers may not call cudaMalloc: code that receives its device buffers from a host
+ * framework that owns all device memory, and serving loops that keep cudaMalloc / cudaFree
+ * out of the step because those calls can block, synchronise the device, or fail mid-step
+ * when memory is tight.  This entry point takes the same arguments as pkv_paged_attention
+ * except the workspace: its scratch is a fixed array of PKV_NOALLOC_SCRATCH_BYTES (16 MiB)
+ * inside the library.  The caller still passes (and owns) every input and the output.
+ *
+ *  - Every GPU that loads the library holds the 16 MiB array until the process exits.
+ *  - The first call on a device (with that device current) looks up the array's device
+ *    address once; make that first call before any stream capture.
+ *  - Sizes whose scratch would exceed PKV_NOALLOC_SCRATCH_BYTES (see
+ *    pkv_paged_attention_workspace_size) are refused with PKV_ERR_WORKSPACE and nothing is
+ *    launched.  Other errors are those of pkv_paged_attention.
+ *  - All calls on a device share the one array, and it keeps the last call's contents
+ *    (nothing in it needs to start at zero).  Calls whose kernels overlap on the GPU (other
+ *    streams, other host threads without ordering) race on it: order them on one stream.
+ *  - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+PKV_API int pkv_paged_attention_noalloc(const void* q_dev, int64_t q_stride_token, int64_t q_stride_head,
+                                        const void* k_cache_dev, const void* v_cache_dev,
+                                        int64_t num_blocks, int64_t block_size,
+                                        const int32_t* block_tables_dev, int64_t block_tables_stride,
+                                        int64_t max_blocks_per_seq,
+                                        const int32_t* context_lens_dev, const int32_t* query_start_loc_dev,
+                                        int64_t num_seqs,
+                                        void* out_dev, int64_t out_stride_token, int64_t out_stride_head,
+                                        int64_t num_tokens, int64_t num_q_heads, int64_t num_kv_heads,
+                                        int64_t head_dim, float scale, void* stream);
+
+/*
  * pkv_set_decode_ctas -- override the number of CTAs the decode split-K kernel uses
  * (0 = automatic: one per SM).  Process-wide; meant for tests and tuning.  Changes the
  * split points, hence rounding, never the result beyond fp32 rounding.  Returns PKV_OK,

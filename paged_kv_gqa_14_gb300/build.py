@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 
-SOURCES = ["abi.cu", "kv_append.cu", "attention.cu"]
+SOURCES = ["abi.cu", "kv_append.cu", "attention.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No --use_fast_math: sincosf in the RoPE kernel stays the accurate library routine; the
 # kernels call fast approximations (ex2.approx) explicitly where they want them.
