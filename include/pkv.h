@@ -207,7 +207,7 @@ PKV_API int pkv_set_decode_ctas(int32_t ctas);
 
 /*
  * pkv_set_decode_kernel -- choose the arithmetic of the decode split-K kernel for later calls:
- * 0 automatic (tensor cores when num_q_heads / num_kv_heads >= 3, else CUDA cores),
+ * 0 automatic (currently the tensor cores for every group size, the faster of the two on GB300),
  * 1 CUDA cores (per-lane fp32 FMA, warp-shuffle reductions),
  * 2 tensor cores (bf16 mma.sync with the GQA group as the N dimension).
  * Both compute the same result up to fp32 rounding.  Process-wide; for tests and tuning.
@@ -221,13 +221,13 @@ PKV_API int pkv_set_decode_kernel(int kind);
  * (both cudaEvent_t passed as void*, created by the caller).  NULL events (or which = 0)
  * switch recording off for that kernel.  Process-wide; meant for benchmarks that time one
  * kernel inside a call.  Returns PKV_ERR_SHAPE for an unknown `which`.
- *   which: 1 kv_append, 2 planner, 3 prefill tiles, 4 decode split-K, 5 split merge.
+ *   which: 1 kv_append, 2 planner, 3 prefill tiles, 4 decode split-K (which also runs the
+ *   split merge of sequences cut by its CTA ranges).
  */
 #define PKV_KERNEL_APPEND 1
 #define PKV_KERNEL_PLAN 2
 #define PKV_KERNEL_PREFILL 3
 #define PKV_KERNEL_DECODE 4
-#define PKV_KERNEL_MERGE 5
 PKV_API int pkv_set_kernel_events(int which, void* start_event, void* stop_event);
 
 /*

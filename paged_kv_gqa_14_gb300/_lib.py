@@ -60,7 +60,7 @@ DEVERR = {
     0x10: "PKV_DEVERR_TIMEOUT",
 }
 
-KERNELS = {"kv_append": 1, "plan": 2, "prefill": 3, "decode": 4, "merge": 5}
+KERNELS = {"kv_append": 1, "plan": 2, "prefill": 3, "decode": 4}
 
 _lib = None
 

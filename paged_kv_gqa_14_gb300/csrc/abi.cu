@@ -20,7 +20,7 @@ unsigned int* g_err_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 std::atomic<int> g_decode_ctas_override{0};
 std::atomic<int> g_decode_kernel{0};
-constexpr int kNumKernels = 6;
+constexpr int kNumKernels = 5;
 std::atomic<void*> g_events[kNumKernels][2];
 
 int current_device() {

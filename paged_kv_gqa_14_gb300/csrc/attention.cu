@@ -6,7 +6,10 @@
 //                                 prefill tile list in the workspace
 //   2. prefill kernel   (persistent) causal varlen tiles for spans longer than one row
 //   3. decode kernel    (1 CTA/SM) split-K over page groups for spans of one row
-//   4. merge_kernel     (B CTAs)  combine the split states of sequences cut by a CTA boundary
+//      ... and the CTA that writes the last split state of a sequence cut by a CTA boundary
+//      merges that sequence's states (the split merge runs inside the decode kernel)
+// Every kernel is launched with programmatic dependent launch, so each one's launch and
+// prologue overlap the previous kernel's tail.
 #include <mutex>
 
 #include "decode.cuh"
@@ -84,6 +87,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   __shared__ int carry[3];
   if (threadIdx.x == 0) carry[0] = carry[1] = carry[2] = 0;
   __syncthreads();
+  pdl_wait();  // the workspace may still be read by the previous call's kernels until now
+  pdl_trigger();
   for (int base = 0; base < num_seqs; base += kPlanThreads) {
     const int b = base + threadIdx.x;
     Int3 v = {0, 0, 0};
@@ -116,6 +121,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     ex.c += carry[2];
     if (v.a) {
       plan.dec_seq[ex.a] = b;
+      plan.dec_count[ex.a] = 0;
       plan.dec_unit[ex.a] = ex.b;
     }
     for (int j = 0; j < v.c; ++j) {
@@ -169,46 +175,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   }
 }
 
-// Merge the split states of each decode sequence cut by a CTA boundary:
-// out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k  (scores are in the log2 domain).
-template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(Plan plan, const int32_t* __restrict__ qsl,
-                                                    bf16* __restrict__ out, int64_t o_st,
-                                                    int64_t o_sh, int hq) {
-  const int i = blockIdx.x;
-  if (i >= plan.header[0]) return;
-  const int chunks = plan.dec_chunks[i];
-  if (chunks <= 1) return;
-  const int slot0 = plan.dec_slot[i];
-  const int64_t t = qsl[plan.dec_seq[i]];
-  constexpr int V = 4;  // dims per thread
-  for (int item = threadIdx.x; item < hq * (D / V); item += blockDim.x) {
-    const int h = item / (D / V);
-    const int d0 = (item - h * (D / V)) * V;
-    float M = -__int_as_float(0x7f800000);
-    for (int k = 0; k < chunks; ++k)
-      M = fmaxf(M, plan.part_ml[(static_cast<int64_t>(slot0 + k) * hq + h) * 2]);
-    float num[V] = {0.f, 0.f, 0.f, 0.f};
-    float den = 0.f;
-    for (int k = 0; k < chunks; ++k) {
-      const int64_t sh = static_cast<int64_t>(slot0 + k) * hq + h;
-      const float2 ml = *reinterpret_cast<const float2*>(plan.part_ml + sh * 2);
-      const float w = fast_exp2(ml.x - M);
-      den = fmaf(w, ml.y, den);
-      const float4 a = *reinterpret_cast<const float4*>(plan.part_acc + sh * D + d0);
-      num[0] = fmaf(w, a.x, num[0]);
-      num[1] = fmaf(w, a.y, num[1]);
-      num[2] = fmaf(w, a.z, num[2]);
-      num[3] = fmaf(w, a.w, num[3]);
-    }
-    const float inv = 1.f / den;
-    uint2 o;
-    o.x = pack_bf16x2(num[0] * inv, num[1] * inv);
-    o.y = pack_bf16x2(num[2] * inv, num[3] * inv);
-    *reinterpret_cast<uint2*>(out + t * o_st + h * o_sh + d0) = o;
-  }
-}
-
 template <int D, int G>
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   using C = DecodeCfg<D, G>;
@@ -241,9 +207,10 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   p.plan = a.plan;
   p.err = a.err;
   record_kernel_event(PKV_KERNEL_DECODE, false, stream);
-  decode_splitk_kernel<D, G><<<a.decode_ctas, (kDecodeWarps + 1) * 32, C::kSmemBytes, stream>>>(p);
+  const cudaError_t e = launch_pdl(decode_splitk_kernel<D, G>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
+                                   C::kSmemBytes, stream, p);
   record_kernel_event(PKV_KERNEL_DECODE, true, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver once (no link-time dependency on libcuda)
@@ -317,9 +284,10 @@ cudaError_t launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
   p.plan = a.plan;
   p.err = a.err;
   record_kernel_event(PKV_KERNEL_DECODE, false, stream);
-  decode_tc_kernel<D, G><<<a.decode_ctas, (kDecodeWarps + 1) * 32, C::kSmemBytes, stream>>>(P);
+  const cudaError_t e = launch_pdl(decode_tc_kernel<D, G>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
+                                   C::kSmemBytes, stream, P);
   record_kernel_event(PKV_KERNEL_DECODE, true, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 template <int D, int G>
@@ -349,24 +317,14 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_tokens == 0) return cudaSuccess;
   const int pps = kDecodeWarps / a.hkv;
   record_kernel_event(PKV_KERNEL_PLAN, false, stream);
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.qsl, a.context_lens, static_cast<int>(a.num_seqs),
-                                               a.num_tokens, a.max_blocks, pps, a.decode_ctas, a.plan,
-                                               a.max_tiles, a.err);
+  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
+                             static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks, pps, a.decode_ctas, a.plan,
+                             a.max_tiles, a.err);
   record_kernel_event(PKV_KERNEL_PLAN, true, stream);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = (a.head_dim == 128) ? launch_prefill<128>(a, stream) : launch_prefill<64>(a, stream);
   if (e != cudaSuccess) return e;
-  e = (a.head_dim == 128) ? launch_decode_g<128>(a, stream) : launch_decode_g<64>(a, stream);
-  if (e != cudaSuccess) return e;
-  const dim3 mgrid(static_cast<unsigned>(a.num_seqs));
-  record_kernel_event(PKV_KERNEL_MERGE, false, stream);
-  if (a.head_dim == 128)
-    merge_kernel<128><<<mgrid, 256, 0, stream>>>(a.plan, a.qsl, static_cast<bf16*>(a.out), a.o_st, a.o_sh, a.hq);
-  else
-    merge_kernel<64><<<mgrid, 256, 0, stream>>>(a.plan, a.qsl, static_cast<bf16*>(a.out), a.o_st, a.o_sh, a.hq);
-  record_kernel_event(PKV_KERNEL_MERGE, true, stream);
-  return cudaGetLastError();
+  return (a.head_dim == 128) ? launch_decode_g<128>(a, stream) : launch_decode_g<64>(a, stream);
 }
 
 // ------------------------------------------------------------------ workspace layout
@@ -393,6 +351,8 @@ PlanSizes plan_sizes(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads, 
   off = align256(off + num_seqs * sizeof(int));
   s.off_dec_chunks = off;
   off = align256(off + num_seqs * sizeof(int));
+  s.off_dec_count = off;
+  off = align256(off + num_seqs * sizeof(int));
   s.off_pf_seq = off;
   off = align256(off + s.max_tiles * sizeof(int));
   s.off_pf_tile = off;
@@ -413,6 +373,7 @@ Plan plan_view(void* workspace, const PlanSizes& s) {
   p.dec_unit = reinterpret_cast<int*>(w + s.off_dec_unit);
   p.dec_slot = reinterpret_cast<int*>(w + s.off_dec_slot);
   p.dec_chunks = reinterpret_cast<int*>(w + s.off_dec_chunks);
+  p.dec_count = reinterpret_cast<int*>(w + s.off_dec_count);
   p.pf_seq = reinterpret_cast<int*>(w + s.off_pf_seq);
   p.pf_tile = reinterpret_cast<int*>(w + s.off_pf_tile);
   p.part_ml = reinterpret_cast<float*>(w + s.off_part_ml);

@@ -113,6 +113,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch (PDL)
+// Every kernel of the library is launched with programmatic stream serialisation, so its
+// launch and prologue overlap the tail of the kernel before it.  pdl_wait() blocks until
+// the preceding grid has completed and its writes are visible; nothing written by an
+// earlier kernel is read before it.  pdl_trigger() lets the next grid start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ integer helpers
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -83,6 +83,51 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, un
   return true;
 }
 
+// Split merge (a6), run inside the decode kernel by the CTA that writes the LAST split state
+// of decode sequence i: out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k (scores are in
+// the log2 domain).  Called by all consumer threads after they wrote this CTA's state.  Each
+// writer publishes its state (fence) before counting itself in dec_count[i]; the CTA that
+// counts last reads every state through L2 and writes the bf16 row.  No thread waits for
+// another CTA, so there is no inter-CTA spin.
+template <int D>
+__device__ void finish_split(const DecodeParams& p, int i, int64_t tq, volatile int* last_flag) {
+  __threadfence();
+  named_bar_sync(1, kDecodeWarps * 32);
+  const int chunks = p.plan.dec_chunks[i];
+  if (threadIdx.x == 0) *last_flag = atomicAdd(&p.plan.dec_count[i], 1) == chunks - 1;
+  named_bar_sync(1, kDecodeWarps * 32);
+  if (*last_flag) {
+    __threadfence();
+    const int slot0 = p.plan.dec_slot[i];
+    for (int item = threadIdx.x; item < p.hq * (D / 4); item += kDecodeWarps * 32) {
+      const int h = item / (D / 4);
+      const int d0 = (item - h * (D / 4)) * 4;
+      float M = -__int_as_float(0x7f800000);
+      for (int k = 0; k < chunks; ++k)
+        M = fmaxf(M, __ldcg(p.plan.part_ml + (static_cast<int64_t>(slot0 + k) * p.hq + h) * 2));
+      float num[4] = {0.f, 0.f, 0.f, 0.f};
+      float den = 0.f;
+      for (int k = 0; k < chunks; ++k) {
+        const int64_t sh = static_cast<int64_t>(slot0 + k) * p.hq + h;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.plan.part_ml + sh * 2));
+        const float w = fast_exp2(ml.x - M);
+        den = fmaf(w, ml.y, den);
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.plan.part_acc + sh * D + d0));
+        num[0] = fmaf(w, a.x, num[0]);
+        num[1] = fmaf(w, a.y, num[1]);
+        num[2] = fmaf(w, a.z, num[2]);
+        num[3] = fmaf(w, a.w, num[3]);
+      }
+      const float inv = 1.f / den;
+      uint2 o;
+      o.x = pack_bf16x2(num[0] * inv, num[1] * inv);
+      o.y = pack_bf16x2(num[2] * inv, num[3] * inv);
+      *reinterpret_cast<uint2*>(p.out + tq * p.o_st + static_cast<int64_t>(h) * p.o_sh + d0) = o;
+    }
+  }
+  named_bar_sync(1, kDecodeWarps * 32);  // last_flag is reused by the next segment
+}
+
 // Load this lane's DPL bf16 of one row and widen to fp32.
 template <int DPL>
 __device__ __forceinline__ void load_row(const bf16* row, int lane, bool valid, float (&x)[DPL]) {
@@ -125,11 +170,22 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   uint64_t* empty = full + STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
   int* seg0 = const_cast<int*>(reinterpret_cast<volatile int*>(abort_flag + 1));
+  volatile int* last_flag = abort_flag + 2;
   float* pbuf = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes + C::kBarBytes);
   float* xbuf = pbuf + kDecodeWarps * 16 * G;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecodeWarps);
+    }
+    fence_mbar_init();
+    *abort_flag = 0;
+  }
+  pdl_wait();  // the plan is written by the planner kernel
+  pdl_trigger();
   const int* hdr = p.plan.header;
   const int n_dec = hdr[0];
   const int U = hdr[1];
@@ -140,12 +196,6 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
 
   const int* dec_unit = p.plan.dec_unit;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kDecodeWarps);
-    }
-    fence_mbar_init();
-    *abort_flag = 0;
     // the decode sequence holding unit ubeg: largest i with dec_unit[i] <= ubeg
     int lo = 0, hi = n_dec - 1;
     while (lo < hi) {
@@ -407,6 +457,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
         }
       }
     }
+    if (p.plan.dec_chunks[i] > 1) finish_split<D>(p, i, tq, last_flag);
     seg_start = true;
     ++i;
   }

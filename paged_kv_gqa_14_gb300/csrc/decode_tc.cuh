@@ -103,10 +103,25 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   uint64_t* empty = full + STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
   int* seg0 = const_cast<int*>(abort_flag + 1);
+  volatile int* last_flag = abort_flag + 2;
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecodeWarps);
+    }
+    fence_mbar_init();
+    *abort_flag = 0;
+  }
+  if (warp == kDecodeWarps && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_v)) : "memory");
+  }
+  pdl_wait();  // the plan is written by the planner kernel
+  pdl_trigger();
   const int* hdr = p.plan.header;
   const int n_dec = hdr[0];
   const int U = hdr[1];
@@ -117,12 +132,6 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
 
   const int* dec_unit = p.plan.dec_unit;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kDecodeWarps);
-    }
-    fence_mbar_init();
-    *abort_flag = 0;
     int lo = 0, hi = n_dec - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -366,6 +375,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
       }
     }
     named_bar_sync(1, kDecodeWarps * 32);
+    if (p.plan.dec_chunks[i] > 1) finish_split<D>(p, i, tq, last_flag);
     seg_start = true;
     ++i;
   }

@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
   constexpr int CH = HALF / 8;  // 16-byte chunks per half head
   __shared__ float2 cs[HALF];
 
+  pdl_wait();  // q, k, v, positions and slots may come from the previous kernel
+  pdl_trigger();
   const int64_t t = blockIdx.x;
   const int64_t pos = positions[t];
   const int64_t slot = slots[t];
@@ -110,20 +112,14 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   for (int i = 0; i < half; ++i) fr.f[i] = pow(a.theta, -2.0 * i / a.head_dim);
   for (int i = half; i < kMaxHeadDim / 2; ++i) fr.f[i] = 0.0;
   const dim3 grid(static_cast<unsigned>(a.num_tokens));
-#define PKV_LAUNCH_APPEND(D)                                                                   \
-  kv_append_kernel<D><<<grid, kAppendThreads, 0, stream>>>(                                    \
-      static_cast<bf16*>(a.q), a.q_st, a.q_sh, static_cast<const bf16*>(a.k), a.k_st, a.k_sh, \
-      static_cast<const bf16*>(a.v), a.v_st, a.v_sh, a.positions, a.slots,                    \
-      static_cast<bf16*>(a.k_cache), static_cast<bf16*>(a.v_cache), a.num_slots, a.hq, a.hkv, \
-      fr, a.err)
   record_kernel_event(PKV_KERNEL_APPEND, false, stream);
-  if (a.head_dim == 128)
-    PKV_LAUNCH_APPEND(128);
-  else
-    PKV_LAUNCH_APPEND(64);
+  const cudaError_t e = launch_pdl(
+      a.head_dim == 128 ? kv_append_kernel<128> : kv_append_kernel<64>, grid, dim3(kAppendThreads), 0, stream,
+      static_cast<bf16*>(a.q), a.q_st, a.q_sh, static_cast<const bf16*>(a.k), a.k_st, a.k_sh,
+      static_cast<const bf16*>(a.v), a.v_st, a.v_sh, a.positions, a.slots, static_cast<bf16*>(a.k_cache),
+      static_cast<bf16*>(a.v_cache), a.num_slots, a.hq, a.hkv, fr, a.err);
   record_kernel_event(PKV_KERNEL_APPEND, true, stream);
-#undef PKV_LAUNCH_APPEND
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace pkv

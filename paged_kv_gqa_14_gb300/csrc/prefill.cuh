@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(128) prefill_kernel(const __grid_constant__ Pr
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, tig = lane & 3;
+  pdl_wait();  // the tile list is written by the planner kernel
+  pdl_trigger();
   const int n_tiles = p.plan.header[3];
   const int total = n_tiles * p.hq;
   const int G = p.hq / p.hkv;
@@ -318,9 +320,9 @@ cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(max_items < cap ? max_items : cap);
   if (grid == 0) return cudaSuccess;
   record_kernel_event(PKV_KERNEL_PREFILL, false, stream);
-  prefill_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+  const cudaError_t e = launch_pdl(prefill_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, p);
   record_kernel_event(PKV_KERNEL_PREFILL, true, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace pkv

@@ -156,7 +156,7 @@ def get_device_error(clear=True, stream=None):
 
 def set_kernel_events(kernel, start=None, stop=None):
     """Record torch.cuda.Event ``start``/``stop`` around every launch of ``kernel``
-    ("kv_append", "plan", "prefill", "decode", "merge"); None switches it off."""
+    ("kv_append", "plan", "prefill", "decode"); None switches it off."""
     which = _lib.KERNELS[kernel]
     for e in (start, stop):
         if e is not None and e.cuda_event == 0:
