@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+from paged_kv_gqa_14_gb300 import replicas  # noqa: E402
 from paged_kv_gqa_14_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention achieved KV GB/s"
@@ -212,6 +213,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     if args.decode_kernel != "auto":
         ops.set_decode_kernel(args.decode_kernel)
+    if args.prefill_kernel != "auto":
+        ops.set_prefill_kernel(args.prefill_kernel)
     dev = torch.device("cuda", local_rank)
     dist = None
     if world > 1:
@@ -256,6 +259,7 @@ def run_gpu(args, rank, world, local_rank):
     K = args.steps
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     dec = [(ev(), ev()) for _ in range(K)]
+    pre = [(ev(), ev()) for _ in range(K)]
     app = [(ev(), ev()) for _ in range(K)]
     att0 = [ev() for _ in range(K)]
     scratch = [ev() for _ in range(K)]
@@ -276,22 +280,22 @@ def run_gpu(args, rank, world, local_rank):
     # (B) the same K steps again with the library recording events around each kernel
     for i in range(K):
         ops.set_kernel_events("decode", *dec[i])
+        ops.set_kernel_events("prefill", *pre[i])
         ops.set_kernel_events("kv_append", *app[i])
         ops.set_kernel_events("plan", att0[i], scratch[i])
         step()
     torch.cuda.synchronize()
     clk = clocks.stop()
     ops.set_kernel_events("decode")
+    ops.set_kernel_events("prefill")
     ops.set_kernel_events("kv_append")
     ops.set_kernel_events("plan")
     total_ms = t_start.elapsed_time(t_stop)
     dec_ms = [a.elapsed_time(b) for a, b in dec]
     app_ms = [a.elapsed_time(b) for a, b in app]
+    pre_ms = [a.elapsed_time(b) for a, b in pre]
     att_ms = [a.elapsed_time(d[1]) for a, d in zip(att0, dec)]  # planner start .. decode end
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replicas.max_over_ranks(total_ms, dist, device=dev)
     ms_step = total_ms / K
     dec_avg = sum(dec_ms) / K
     peak, peak_kind = hbm_peak()
@@ -350,15 +354,12 @@ def run_gpu(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = replicas.max_over_ranks(e2e_ms, dist, device=dev)
     assert ops.get_device_error() == 0, "device error during timing"
 
     line = {
         "metric": METRIC,
-        "value": round(world * kv_u / (ms_step * 1e-3) / 1e9, 2),
+        "value": round(replicas.job_throughput(kv_u, world, ms_step * 1e-3) / 1e9, 2),
         "unit": UNIT,
         "n_gpus": world,
         "steps": K,
@@ -381,6 +382,7 @@ def run_gpu(args, rank, world, local_rank):
             "new_tokens": bt.num_tokens,
             "parallelism": f"replicas x{world}",
             "decode_kernel": args.decode_kernel,
+            "prefill_kernel": args.prefill_kernel,
             "l2": "inputs larger than L2 (unique KV per step %.0f MB > 129 MB); no flush" % (kv_u / 1e6),
         },
         "tokens_per_s_per_layer": round(world * bt.num_tokens / (ms_step * 1e-3), 1),
@@ -392,6 +394,7 @@ def run_gpu(args, rank, world, local_rank):
             "kv_append": round(sum(app_ms) / K, 5),
             "paged_attention_call": round(sum(att_ms) / K, 5),
             "decode_splitk": round(dec_avg, 5),
+            "prefill_tiles": round(sum(pre_ms) / K, 5),
         },
         "roofline": {
             "kernel": "decode_splitk",
@@ -485,14 +488,13 @@ def main():
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--seqs", type=int, default=0, help="only the first N sequences (small profiling case)")
     ap.add_argument("--decode-kernel", choices=["auto", "simt", "tensor"], default="auto")
+    ap.add_argument("--prefill-kernel", choices=["auto", "mma", "tcgen05"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local_rank = replicas.rank_info()
     if args.impl == "reference":
         if rank != 0:
             return

@@ -113,6 +113,30 @@ PKV_API int pkv_kv_append(void* q_dev, int64_t q_stride_token, int64_t q_stride_
                   double rope_theta, void* stream);
 
 /*
+ * pkv_kv_append_paged -- pkv_kv_append with each token's position and slot derived on the
+ * device from the scheduler's tables instead of passed in ("mini-vllm" README, "Milestones",
+ * 7: GPU-side slot derivation).  Token t belongs to the sequence b whose span
+ * [query_start_loc[b], query_start_loc[b+1]) contains it; it sits at position
+ * pos = context_lens[b] - span_b + (t - query_start_loc[b]) and is written to slot
+ * block_tables[b][pos / 16] * 16 + pos % 16.  Tokens outside every span are only rotated
+ * (q) and write nothing.  Inconsistent tables set PKV_DEVERR_SPAN / _CONTEXT / _BLOCK_RANGE
+ * and skip the token's K/V write.  Table arguments as in pkv_paged_attention; the others as in
+ * pkv_kv_append.  positions_out / slot_mapping_out (int64 [num_tokens], may be NULL) receive
+ * the derived values (-1 slot for skipped tokens).
+ */
+PKV_API int pkv_kv_append_paged(void* q_dev, int64_t q_stride_token, int64_t q_stride_head,
+                                const void* k_dev, int64_t k_stride_token, int64_t k_stride_head,
+                                const void* v_dev, int64_t v_stride_token, int64_t v_stride_head,
+                                const int32_t* block_tables_dev, int64_t block_tables_stride,
+                                int64_t max_blocks_per_seq,
+                                const int32_t* context_lens_dev, const int32_t* query_start_loc_dev,
+                                int64_t num_seqs, void* k_cache_dev, void* v_cache_dev,
+                                int64_t num_tokens, int64_t num_q_heads, int64_t num_kv_heads,
+                                int64_t head_dim, int64_t num_blocks, int64_t block_size,
+                                double rope_theta, int64_t* positions_out_dev,
+                                int64_t* slot_mapping_out_dev, void* stream);
+
+/*
  * pkv_paged_attention_workspace_size -- bytes of device workspace pkv_paged_attention needs
  * for these sizes on the current device (the split-K partials and the work plan).
  * Returns 0 if the sizes are invalid.  The result depends on the device's SM count and on
@@ -214,6 +238,15 @@ PKV_API int pkv_set_decode_ctas(int32_t ctas);
  * Returns PKV_ERR_SHAPE for another value.
  */
 PKV_API int pkv_set_decode_kernel(int kind);
+
+/*
+ * pkv_set_prefill_kernel -- choose the arithmetic of the prefill-chunk tiles for later calls:
+ * 0 automatic (currently 2), 1 bf16 mma.sync tiles of 64 query rows, 2 tcgen05 tiles of 128
+ * query rows (TMEM accumulators, TMA-staged operands; falls back to 1 when q's strides do
+ * not admit a TMA tensor map).  Both compute the same result up to fp32 rounding.
+ * Process-wide; for tests and tuning.  Returns PKV_ERR_SHAPE for another value.
+ */
+PKV_API int pkv_set_prefill_kernel(int kind);
 
 /*
  * pkv_set_kernel_events -- instrumentation: from now on, every launch of kernel `which`

@@ -23,6 +23,11 @@ SIGNATURES = {
         [_c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p,
          _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_double, _c_p],
     ),
+    "pkv_kv_append_paged": (
+        ctypes.c_int,
+        [_c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_p,
+         _c_i64, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_double, _c_p, _c_p, _c_p],
+    ),
     "pkv_paged_attention_workspace_size": (ctypes.c_size_t, [_c_i64] * 6),
     "pkv_paged_attention": (
         ctypes.c_int,
@@ -37,6 +42,7 @@ SIGNATURES = {
     ),
     "pkv_set_decode_ctas": (ctypes.c_int, [ctypes.c_int32]),
     "pkv_set_decode_kernel": (ctypes.c_int, [ctypes.c_int]),
+    "pkv_set_prefill_kernel": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_kernel_events": (ctypes.c_int, [ctypes.c_int, _c_p, _c_p]),
     "pkv_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _c_p]),
 }

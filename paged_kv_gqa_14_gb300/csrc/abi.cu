@@ -20,6 +20,7 @@ unsigned int* g_err_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 std::atomic<int> g_decode_ctas_override{0};
 std::atomic<int> g_decode_kernel{0};
+std::atomic<int> g_prefill_kernel{0};
 constexpr int kNumKernels = 5;
 std::atomic<void*> g_events[kNumKernels][2];
 
@@ -67,6 +68,13 @@ void record_kernel_event(int which, bool after, cudaStream_t stream) {
 
 int decode_kernel_choice() { return g_decode_kernel.load(); }
 
+// Automatic choice: the tcgen05 tiles (65 us vs 113 us for the mma.sync tiles on the
+// mixed chunked-prefill workload on GB300).
+int prefill_kernel_choice() {
+  const int k = g_prefill_kernel.load();
+  return k == 0 ? 2 : k;
+}
+
 int decode_ctas_for_device() {
   const int o = g_decode_ctas_override.load();
   if (o > 0) return o;
@@ -107,6 +115,12 @@ int pkv_set_decode_kernel(int kind) {
   return PKV_OK;
 }
 
+int pkv_set_prefill_kernel(int kind) {
+  if (kind < 0 || kind > 2) return PKV_ERR_SHAPE;
+  g_prefill_kernel.store(kind);
+  return PKV_OK;
+}
+
 int pkv_set_kernel_events(int which, void* start_event, void* stop_event) {
   if (which < 0 || which >= kNumKernels) return PKV_ERR_SHAPE;
   if (which == 0) {
@@ -138,7 +152,7 @@ int pkv_kv_append(void* q, int64_t q_st, int64_t q_sh, const void* k, int64_t k_
   if ((q_st | q_sh | k_st | k_sh | v_st | v_sh) & 7) return PKV_ERR_ALIGN;
   const int dev = current_device();
   if (!device_setup(dev)) return PKV_ERR_CUDA;
-  AppendArgs a;
+  AppendArgs a{};
   a.q = q;
   a.q_st = q_st;
   a.q_sh = q_sh;
@@ -150,6 +164,61 @@ int pkv_kv_append(void* q, int64_t q_st, int64_t q_sh, const void* k, int64_t k_
   a.v_sh = v_sh;
   a.positions = positions;
   a.slots = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_tokens = num_tokens;
+  a.num_slots = num_blocks * kBlockSize;
+  a.hq = static_cast<int>(num_q_heads);
+  a.hkv = static_cast<int>(num_kv_heads);
+  a.head_dim = static_cast<int>(head_dim);
+  a.theta = rope_theta;
+  a.err = g_err_ptr[dev];
+  return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_kv_append_paged(void* q, int64_t q_st, int64_t q_sh, const void* k, int64_t k_st, int64_t k_sh,
+                        const void* v, int64_t v_st, int64_t v_sh, const int32_t* block_tables, int64_t bt_stride,
+                        int64_t max_blocks_per_seq, const int32_t* context_lens, const int32_t* query_start_loc,
+                        int64_t num_seqs, void* k_cache, void* v_cache, int64_t num_tokens, int64_t num_q_heads,
+                        int64_t num_kv_heads, int64_t head_dim, int64_t num_blocks, int64_t block_size,
+                        double rope_theta, int64_t* positions_out, int64_t* slot_mapping_out, void* stream) {
+  if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
+      max_blocks_per_seq < 0)
+    return PKV_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads) return PKV_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (!(rope_theta > 0.0)) return PKV_ERR_SHAPE;
+  if (num_seqs > (1 << 30)) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!q || !k || !v || !block_tables || !context_lens || !query_start_loc || !k_cache || !v_cache)
+    return PKV_ERR_NULL;
+  if (bt_stride < max_blocks_per_seq) return PKV_ERR_STRIDE;
+  if (q_st < 0 || q_sh < 0 || k_st < 0 || k_sh < 0 || v_st < 0 || v_sh < 0) return PKV_ERR_STRIDE;
+  if (!rows_disjoint(num_tokens, q_st, num_q_heads, q_sh, head_dim)) return PKV_ERR_STRIDE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ALIGN;
+  if ((q_st | q_sh | k_st | k_sh | v_st | v_sh) & 7) return PKV_ERR_ALIGN;
+  const int dev = current_device();
+  if (!device_setup(dev)) return PKV_ERR_CUDA;
+  AppendArgs a{};
+  a.q = q;
+  a.q_st = q_st;
+  a.q_sh = q_sh;
+  a.k = k;
+  a.k_st = k_st;
+  a.k_sh = k_sh;
+  a.v = v;
+  a.v_st = v_st;
+  a.v_sh = v_sh;
+  a.qsl = query_start_loc;
+  a.context_lens = context_lens;
+  a.block_tables = block_tables;
+  a.bt_stride = bt_stride;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.positions_out = positions_out;
+  a.slots_out = slot_mapping_out;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.num_tokens = num_tokens;
@@ -227,6 +296,7 @@ int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k
   a.scale = scale;
   a.decode_ctas = ctas;
   a.decode_kernel = decode_kernel_choice();
+  a.prefill_kernel = prefill_kernel_choice();
   a.plan = plan_view(workspace, ps);
   a.max_tiles = ps.max_tiles;
   a.err = g_err_ptr[dev];

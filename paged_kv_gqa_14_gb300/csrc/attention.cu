@@ -15,6 +15,7 @@
 #include "decode.cuh"
 #include "decode_tc.cuh"
 #include "prefill.cuh"
+#include "prefill_tc.cuh"
 
 namespace pkv {
 namespace {
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             const int32_t* __restrict__ ctxl,
                                                             int num_seqs, int64_t num_tokens,
                                                             int64_t max_blocks, int pps,
-                                                            int decode_ctas, Plan plan,
+                                                            int decode_ctas, int tile_q, Plan plan,
                                                             int64_t max_tiles, unsigned int* err) {
   __shared__ int sm[3 * 32];
   __shared__ int carry[3];
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         v.a = 1;
         v.b = ceil_div(ceil_div(ctx, kBlockSize), pps);
       }
-      if (ok && span > 1) v.c = ceil_div(span, kPrefillTileQ);
+      if (ok && span > 1) v.c = ceil_div(span, tile_q);
     }
     Int3 tot;
     Int3 ex = block_scan3(v, tot, sm);
@@ -311,18 +312,70 @@ cudaError_t launch_decode_g(const AttnArgs& a, cudaStream_t stream) {
   }
 }
 
+// q [T][Hq][d] as a 3-D tensor {d, Hq, T}; a box is 128 token rows x 64 dims of one head.
+bool make_q_map(CUtensorMap* m, const AttnArgs& a) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.head_dim), static_cast<cuuint64_t>(a.hq),
+                              static_cast<cuuint64_t>(a.num_tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.q_sh) * 2, static_cast<cuuint64_t>(a.q_st) * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_prefill_tc_params(const AttnArgs& a, PrefillTcParams* P) {
+  if (a.q_sh <= 0 || a.q_st <= 0) return false;
+  if (!make_q_map(&P->tmap_q, a) || !make_pool_map(&P->tmap_k, a.k_cache, a.num_blocks, a.hkv, a.head_dim) ||
+      !make_pool_map(&P->tmap_v, a.v_cache, a.num_blocks, a.hkv, a.head_dim))
+    return false;
+  P->p = make_prefill_params(a);
+  return true;
+}
+
+template <int D>
+cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaStream_t stream) {
+  using C = PrefillTcCfg<D>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int64_t max_items = (a.num_tokens / C::BQ + a.num_seqs + 1) * a.hq;
+  const int64_t cap = device_sm_count();
+  const unsigned grid = static_cast<unsigned>(max_items < cap ? max_items : cap);
+  record_kernel_event(PKV_KERNEL_PREFILL, false, stream);
+  const cudaError_t e = launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(256), C::kSmemBytes, stream, P);
+  record_kernel_event(PKV_KERNEL_PREFILL, true, stream);
+  return e;
+}
+
 }  // namespace
 
 cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_tokens == 0) return cudaSuccess;
   const int pps = kDecodeWarps / a.hkv;
+  // prefill arithmetic: tcgen05 (128-row tiles) when chosen and its q tensor map encodes,
+  // else mma.sync (64-row tiles)
+  PrefillTcParams tcp;
+  const bool use_tc = a.prefill_kernel == 2 && make_prefill_tc_params(a, &tcp);
+  const int tile_q = use_tc ? PrefillTcCfg<128>::BQ : kPrefillTileQ;
   record_kernel_event(PKV_KERNEL_PLAN, false, stream);
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
-                             static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks, pps, a.decode_ctas, a.plan,
-                             a.max_tiles, a.err);
+                             static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks, pps, a.decode_ctas, tile_q,
+                             a.plan, a.max_tiles, a.err);
   record_kernel_event(PKV_KERNEL_PLAN, true, stream);
   if (e != cudaSuccess) return e;
-  e = (a.head_dim == 128) ? launch_prefill<128>(a, stream) : launch_prefill<64>(a, stream);
+  if (use_tc)
+    e = (a.head_dim == 128) ? launch_prefill_tc<128>(a, tcp, stream) : launch_prefill_tc<64>(a, tcp, stream);
+  else
+    e = (a.head_dim == 128) ? launch_prefill<128>(a, stream) : launch_prefill<64>(a, stream);
   if (e != cudaSuccess) return e;
   return (a.head_dim == 128) ? launch_decode_g<128>(a, stream) : launch_decode_g<64>(a, stream);
 }

@@ -61,8 +61,14 @@ struct AppendArgs {
   int64_t k_st, k_sh;
   const void* v;
   int64_t v_st, v_sh;
-  const int64_t* positions;
+  const int64_t* positions;  // explicit positions / slots, or
   const int64_t* slots;
+  const int32_t* qsl;           // (non-null) derive them from the scheduler's tables
+  const int32_t* context_lens;
+  const int32_t* block_tables;
+  int64_t bt_stride, max_blocks, num_seqs;
+  int64_t* positions_out;       // optional copies of the derived values
+  int64_t* slots_out;
   void* k_cache;
   void* v_cache;
   int64_t num_tokens, num_slots;
@@ -89,7 +95,8 @@ struct AttnArgs {
   int hq, hkv, head_dim;
   float scale;
   int decode_ctas;
-  int decode_kernel;  // 0 automatic, 1 CUDA-core (warp-shuffle), 2 tensor-core (mma.sync)
+  int decode_kernel;   // 0 automatic, 1 CUDA-core (warp-shuffle), 2 tensor-core (mma.sync)
+  int prefill_kernel;  // 1 mma.sync tiles, 2 tcgen05 tiles (resolved from the process setting)
   Plan plan;
   int64_t max_tiles;
   unsigned int* err;
@@ -122,5 +129,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 void record_kernel_event(int which, bool after, cudaStream_t stream);
 int decode_ctas_for_device();
 int decode_kernel_choice();
+int prefill_kernel_choice();
 
 }  // namespace pkv

@@ -17,6 +17,19 @@ namespace {
 
 constexpr int kAppendThreads = 128;
 
+// Where each token's position and slot come from: explicit arrays, or (qsl != nullptr)
+// derived on the device from the scheduler's tables.
+struct AppendSrc {
+  const int64_t* positions;
+  const int64_t* slots;
+  const int32_t* qsl;
+  const int32_t* ctxl;
+  const int32_t* bt;
+  int64_t bt_stride, max_blocks, num_seqs;
+  int64_t* pos_out;
+  int64_t* slot_out;
+};
+
 struct RopeFreqs {
   double f[kMaxHeadDim / 2];  // f_i = theta^(-2 i / d), i < d/2
 };
@@ -38,22 +51,89 @@ __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float2* cs) 
   }
 }
 
+// Position and slot of token t, derived on the device from the scheduler's tables: the
+// token's sequence b is the last one with query_start_loc[b] <= t (found by a warp-wide
+// search, 32 samples per round), it sits at position ctx_b - n_b + (t - qsl[b]) and its slot
+// is row pos % 16 of block block_tables[b][pos / 16].  Tokens outside every span get slot -1.
+__device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t num_blocks, unsigned int* err,
+                            int64_t& pos, int64_t& slot) {
+  const int32_t* qsl = src.qsl;
+  int lo = 0, hi = static_cast<int>(src.num_seqs);  // inclusive range of qsl indices
+  int b = -1;
+  for (int round = 0; round < 8; ++round) {  // 32^8 covers any int32 count
+    const int len = hi - lo + 1;
+    if (len <= 32) {
+      const int idx = lo + lane;
+      const unsigned m = __ballot_sync(0xffffffffu, idx <= hi && qsl[idx] <= t);
+      b = lo + __popc(m) - 1;
+      break;
+    }
+    const int stride = (len + 31) / 32;
+    const int idx = min(lo + lane * stride, hi);
+    const unsigned m = __ballot_sync(0xffffffffu, qsl[idx] <= t);
+    const int k = __popc(m) - 1;
+    if (k < 0) break;
+    const int nlo = lo + k * stride;
+    hi = min(hi, nlo + stride - 1);
+    lo = nlo;
+  }
+  pos = 0;
+  slot = -1;
+  if (b < 0 || b >= src.num_seqs) return;  // before the first or after the last span
+  const int s0 = qsl[b];
+  const int n = qsl[b + 1] - s0;
+  const int ctx = src.ctxl[b];
+  if (n <= 0 || t - s0 >= n) return;
+  if (ctx < n) {
+    if (lane == 0) raise_error(err, PKV_DEVERR_SPAN);
+    return;
+  }
+  pos = static_cast<int64_t>(ctx) - n + (t - s0);
+  const int64_t page = pos / 16;
+  if (page >= src.max_blocks) {
+    if (lane == 0) raise_error(err, PKV_DEVERR_CONTEXT);
+    return;
+  }
+  const int blk = src.bt[static_cast<int64_t>(b) * src.bt_stride + page];
+  if (blk < 0 || blk >= num_blocks) {
+    if (lane == 0) raise_error(err, PKV_DEVERR_BLOCK_RANGE);
+    return;
+  }
+  slot = static_cast<int64_t>(blk) * 16 + pos % 16;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
     bf16* __restrict__ q, int64_t q_st, int64_t q_sh, const bf16* __restrict__ k, int64_t k_st,
-    int64_t k_sh, const bf16* __restrict__ v, int64_t v_st, int64_t v_sh,
-    const int64_t* __restrict__ positions, const int64_t* __restrict__ slots,
+    int64_t k_sh, const bf16* __restrict__ v, int64_t v_st, int64_t v_sh, const __grid_constant__ AppendSrc src,
     bf16* __restrict__ k_cache, bf16* __restrict__ v_cache, int64_t num_slots, int hq, int hkv,
     const __grid_constant__ RopeFreqs fr, unsigned int* err) {
   constexpr int HALF = D / 2;
   constexpr int CH = HALF / 8;  // 16-byte chunks per half head
   __shared__ float2 cs[HALF];
+  __shared__ int64_t s_pos, s_slot;
 
-  pdl_wait();  // q, k, v, positions and slots may come from the previous kernel
+  pdl_wait();  // q, k, v and the index inputs may come from the previous kernel
   pdl_trigger();
   const int64_t t = blockIdx.x;
-  const int64_t pos = positions[t];
-  const int64_t slot = slots[t];
+  if (threadIdx.x < 32) {
+    int64_t p_, s_;
+    if (src.qsl) {
+      derive_slot(src, t, threadIdx.x, num_slots / 16, err, p_, s_);
+    } else {
+      p_ = src.positions[t];
+      s_ = src.slots[t];
+    }
+    if (threadIdx.x == 0) {
+      s_pos = p_;
+      s_slot = s_;
+      if (src.pos_out) src.pos_out[t] = p_;
+      if (src.slot_out) src.slot_out[t] = s_;
+    }
+  }
+  __syncthreads();
+  const int64_t pos = s_pos;
+  const int64_t slot = s_slot;
 
   for (int i = threadIdx.x; i < HALF; i += kAppendThreads) {
     const double a = static_cast<double>(pos) * fr.f[i];
@@ -112,11 +192,22 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   for (int i = 0; i < half; ++i) fr.f[i] = pow(a.theta, -2.0 * i / a.head_dim);
   for (int i = half; i < kMaxHeadDim / 2; ++i) fr.f[i] = 0.0;
   const dim3 grid(static_cast<unsigned>(a.num_tokens));
+  AppendSrc src;
+  src.positions = a.positions;
+  src.slots = a.slots;
+  src.qsl = a.qsl;
+  src.ctxl = a.context_lens;
+  src.bt = a.block_tables;
+  src.bt_stride = a.bt_stride;
+  src.max_blocks = a.max_blocks;
+  src.num_seqs = a.num_seqs;
+  src.pos_out = a.positions_out;
+  src.slot_out = a.slots_out;
   record_kernel_event(PKV_KERNEL_APPEND, false, stream);
   const cudaError_t e = launch_pdl(
       a.head_dim == 128 ? kv_append_kernel<128> : kv_append_kernel<64>, grid, dim3(kAppendThreads), 0, stream,
       static_cast<bf16*>(a.q), a.q_st, a.q_sh, static_cast<const bf16*>(a.k), a.k_st, a.k_sh,
-      static_cast<const bf16*>(a.v), a.v_st, a.v_sh, a.positions, a.slots, static_cast<bf16*>(a.k_cache),
+      static_cast<const bf16*>(a.v), a.v_st, a.v_sh, src, static_cast<bf16*>(a.k_cache),
       static_cast<bf16*>(a.v_cache), a.num_slots, a.hq, a.hkv, fr, a.err);
   record_kernel_event(PKV_KERNEL_APPEND, true, stream);
   return e;

@@ -35,6 +35,13 @@ struct PrefillParams {
   unsigned int* err;
 };
 
+// Persistent grids walk the work list heaviest first (the planner lists each span's tiles in
+// order, later tiles see more keys) in a snake: even waves left to right, odd waves right to
+// left, so the CTA that took the heaviest item of one wave takes the lightest of the next.
+__device__ __forceinline__ int snake_order(int wave, int cta, int ctas) {
+  return wave * ctas + ((wave & 1) ? ctas - 1 - cta : cta);
+}
+
 template <int D>
 struct PrefillCfg {
   static constexpr int TQ = kPrefillTileQ;  // q rows per work item
@@ -132,8 +139,10 @@ __global__ void __launch_bounds__(128) prefill_kernel(const __grid_constant__ Pr
   const int total = n_tiles * p.hq;
   const int G = p.hq / p.hkv;
 
-  for (int w = blockIdx.x; w < total; w += gridDim.x) {
-    const int item = total - 1 - w;  // later (longer) tiles of each span first
+  for (int wave = 0; wave * static_cast<int>(gridDim.x) < total; ++wave) {
+    const int ord = snake_order(wave, blockIdx.x, gridDim.x);
+    if (ord >= total) continue;
+    const int item = total - 1 - ord;  // later (longer) tiles of each span first
     const int ti = item / p.hq;
     const int hq = item - ti * p.hq;
     const int h = hq / G;
@@ -284,18 +293,7 @@ __global__ void __launch_bounds__(128) prefill_kernel(const __grid_constant__ Pr
   }
 }
 
-template <int D>
-cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream) {
-  using C = PrefillCfg<D>;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+inline PrefillParams make_prefill_params(const AttnArgs& a) {
   PrefillParams p;
   p.q = static_cast<const bf16*>(a.q);
   p.q_st = a.q_st;
@@ -315,6 +313,22 @@ cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream) {
   p.qscale = a.scale * 1.4426950408889634f;
   p.plan = a.plan;
   p.err = a.err;
+  return p;
+}
+
+template <int D>
+cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream) {
+  using C = PrefillCfg<D>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const PrefillParams p = make_prefill_params(a);
   const int64_t max_items = a.max_tiles * a.hq;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 2;
   const unsigned grid = static_cast<unsigned>(max_items < cap ? max_items : cap);

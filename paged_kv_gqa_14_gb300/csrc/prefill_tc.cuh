@@ -1,0 +1,409 @@
+// Prefill-chunk attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Same work items and causal rule as prefill.cuh ("mini_engine" README, "What it does":
+// chunked prefill; "09 -- Mini Inference Engine (The Capstone)", "Week 3": mixed batches):
+// an item is (sequence, 128-row tile of its span, q head); row r of an n-row span sits at
+// position ctx - n + r and sees keys 0 .. ctx - n + r.
+//
+// Per item, one CTA of eight warps with fixed roles:
+//   warp 0     TMA producer: the Q tile once (3-D tensor map over q), then K and V tiles of
+//              128 keys = 8 pages gathered through the block table (4-D pool map, one box
+//              per page x kv head x 64 dims), into a 2-stage ring.
+//   warp 1     allocates TMEM (S double buffer: 2 x 128 columns; O: d columns) and, from one
+//              thread, issues   S = Q . K^T   (M 128, N 128, K d)   and
+//                               O += P . V    (M 128, N d,   K 128)  as tcgen05.mma kind::f16,
+//              bf16 operands from shared memory, fp32 accumulators in TMEM, completion
+//              signalled with tcgen05.commit on mbarriers.
+//   warps 2-3  transpose each V tile into V^T (ldmatrix.trans / stmatrix) so that both
+//              operands of every MMA are K-major; keys past the visible range become 0.
+//   warps 4-7  softmax: thread = query row.  Reads its S row from TMEM, masks by select,
+//              keeps a running max m and sum l in the log2 domain and writes P (bf16) to
+//              shared memory.  O in TMEM is rescaled only when the row max grows by more
+//              than 2^8 (the stale max stays the reference otherwise; O and l share it, so the
+//              result is unchanged).  At the end it reads O, divides by l and stores bf16.
+// Every wait is bounded; a CTA that times out sets PKV_DEVERR_TIMEOUT and finishes its items
+// without further work.
+#pragma once
+
+#include <cuda.h>
+
+#include "decode_tc.cuh"
+#include "prefill.cuh"
+#include "tcgen05.cuh"
+
+namespace pkv {
+
+struct PrefillTcParams {
+  CUtensorMap tmap_q;  // 3-D {d, Hq, T}, box {64, 1, 128}, 128B swizzle
+  CUtensorMap tmap_k;  // 4-D {d, Hkv, 16, num_blocks}, box {64, 1, 16, 1}, 128B swizzle
+  CUtensorMap tmap_v;
+  PrefillParams p;
+};
+
+template <int D>
+struct PrefillTcCfg {
+  static constexpr int BQ = 128;  // query rows per item
+  static constexpr int BK = 128;  // keys per K/V tile (8 pages)
+  static constexpr int HALVES = D / 64;
+  static constexpr int kBlk = 128 * 128;  // one [128 rows][64 elements] swizzled block: 16 KB
+  static constexpr int kQBytes = BQ * D * 2;
+  static constexpr int kKVBytes = BK * D * 2;
+  static constexpr int kVtBytes = D * BK * 2;
+  static constexpr int kPBytes = BQ * BK * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + kQBytes;       // 2 stages
+  static constexpr int OFF_V = OFF_K + 2 * kKVBytes;  // 2 stages
+  static constexpr int OFF_VT = OFF_V + 2 * kKVBytes;
+  static constexpr int OFF_P = OFF_VT + kVtBytes;
+  static constexpr int OFF_BAR = OFF_P + kPBytes;
+  static constexpr int kSmemBytes = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_O = 256;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+// All 32 lanes wait; the outcome is made warp-uniform (any lane timing out aborts the warp).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                          volatile int* abort_flag) {
+  const bool ok = wait_or_abort(bar, parity, err, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams P) {
+  using C = PrefillTcCfg<D>;
+  constexpr int HALVES = C::HALVES;
+  const PrefillParams& p = P.p;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* v_full = bars + 3;   // [2]
+  uint64_t* k_empty = bars + 5;  // [2] MMA finished reading the K stage
+  uint64_t* v_empty = bars + 7;  // [2] transposers finished reading the V stage
+  uint64_t* s_full = bars + 9;   // [2] S buffer written
+  uint64_t* s_free = bars + 11;  // [2] softmax finished reading the S buffer
+  uint64_t* vt_full = bars + 13;
+  uint64_t* p_full = bars + 14;
+  uint64_t* pv_done = bars + 15;
+  uint64_t* fin = bars + 16;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  const float NEG_INF = -__int_as_float(0x7f800000);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 2);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 4);
+    }
+    mbar_init(vt_full, 2);
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(fin, 1);
+    fence_mbar_init();
+    *abort_flag = 0;
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_q)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_v)) : "memory");
+  }
+  if (warp == 1) {
+    tc5::alloc(tmem_slot, C::TMEM_COLS);
+    tc5::relinquish();
+  }
+  tc5::fence_before();
+  __syncthreads();
+  tc5::fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_wait();  // the tile list is written by the planner kernel
+  pdl_trigger();
+  const int n_tiles = p.plan.header[3];
+  const int total = n_tiles * p.hq;
+  const int G = p.hq / p.hkv;
+  const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by the other items
+
+  int t_glob = 0;  // K/V tiles this CTA has processed (ring slots, S buffers, PV phases)
+  int item_no = 0;
+  for (int wave = 0; wave * static_cast<int>(gridDim.x) < total; ++wave) {
+    const int ord = snake_order(wave, blockIdx.x, gridDim.x);
+    if (ord >= total) continue;
+    const int item = total - 1 - ord;  // later (longer) tiles of each span first
+    const int ti = item / p.hq;
+    const int hq = item - ti * p.hq;
+    const int h = hq / G;
+    const int b = p.plan.pf_seq[ti];
+    const int j = p.plan.pf_tile[ti];
+    const int s0 = p.qsl[b];
+    const int n = p.qsl[b + 1] - s0;
+    const int ctx = p.context_lens[b];
+    const int q0 = j * C::BQ;
+    const int qrows = min(C::BQ, n - q0);
+    const int pos0 = ctx - n + q0;
+    const int kv_end = pos0 + qrows;  // keys [0, kv_end) are visible to some row
+    const int nkt = ceil_div(kv_end, C::BK);
+    const int npages = ceil_div(kv_end, 16);
+
+    if (warp == 0) {
+      // ------------------------------------------------------------------ TMA producer
+      bool ok = !*abort_flag;
+      if (ok) {
+        if (lane == 0) mbar_arrive_expect_tx(q_full, C::kQBytes);
+        __syncwarp();
+        if (lane < HALVES) tma_load_3d(smem + C::OFF_Q + lane * C::kBlk, &P.tmap_q, lane * 64, hq, s0 + q0, q_full);
+      }
+      const int per = 8 * HALVES;  // boxes per K (or V) tile
+      const int kv = lane / per;
+      const int rem = lane - kv * per;
+      const int pg = rem / HALVES;
+      const int half = rem - pg * HALVES;
+      for (int jt = 0; jt < nkt && ok; ++jt) {
+        const int f = t_glob + jt;
+        const int s = f & 1;
+        if (f >= 2) {
+          ok = warp_wait(&k_empty[s], ((f >> 1) - 1) & 1, p.err, abort_flag) &&
+               warp_wait(&v_empty[s], ((f >> 1) - 1) & 1, p.err, abort_flag);
+          if (!ok) break;
+        }
+        const int npg = min(8, npages - jt * 8);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&k_full[s], static_cast<uint32_t>(npg * HALVES * 2048));
+          mbar_arrive_expect_tx(&v_full[s], static_cast<uint32_t>(npg * HALVES * 2048));
+        }
+        __syncwarp();
+        if (lane < 2 * per && pg < npg) {
+          int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + jt * 8 + pg];
+          if (blk < 0 || blk >= p.num_blocks) {
+            raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+            blk = 0;
+          }
+          unsigned char* dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::kKVBytes + half * C::kBlk + pg * 2048;
+          tma_load_4d(dst, kv ? &P.tmap_v : &P.tmap_k, half * 64, h, 0, blk, kv ? &v_full[s] : &k_full[s], pol);
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t kIdescQK = tc5::idesc_bf16_f32(128, 128);
+        constexpr uint32_t kIdescPV = tc5::idesc_bf16_f32(128, D);
+        bool ok = wait_or_abort(q_full, item_no & 1, p.err, abort_flag);
+        auto issue_pv = [&](int fp, bool first) -> bool {
+          if (!wait_or_abort(vt_full, fp & 1, p.err, abort_flag)) return false;
+          if (!wait_or_abort(p_full, fp & 1, p.err, abort_flag)) return false;
+          tc5::fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlk + (kk & 3) * 32;
+            const uint32_t offv = (kk >> 2) * (D * 128) + (kk & 3) * 32;
+            tc5::mma_ss(tmem + C::COL_O, tc5::smem_desc_k128(sb + C::OFF_P + off),
+                        tc5::smem_desc_k128(sb + C::OFF_VT + offv), kIdescPV, (first && kk == 0) ? 0u : 1u);
+          }
+          tc5::commit(pv_done);
+          return true;
+        };
+        for (int jt = 0; jt < nkt && ok; ++jt) {
+          const int f = t_glob + jt;
+          const int s = f & 1;
+          ok = wait_or_abort(&k_full[s], (f >> 1) & 1, p.err, abort_flag);
+          if (ok && f >= 2) ok = wait_or_abort(&s_free[s], ((f >> 1) - 1) & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc5::fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlk + (kk & 3) * 32;
+            tc5::mma_ss(tmem + 128u * s, tc5::smem_desc_k128(sb + C::OFF_Q + off),
+                        tc5::smem_desc_k128(sb + C::OFF_K + s * C::kKVBytes + off), kIdescQK, kk > 0 ? 1u : 0u);
+          }
+          tc5::commit(&s_full[s]);
+          tc5::commit(&k_empty[s]);
+          if (jt > 0) ok = issue_pv(f - 1, jt == 1);
+        }
+        if (ok) issue_pv(t_glob + nkt - 1, nkt == 1);
+      }
+      __syncwarp();
+    } else if (warp < 4) {
+      // ------------------------------------------------------- V -> V^T transposers
+      const int tw = warp - 2;
+      bool ok = !*abort_flag;
+      for (int jt = 0; jt < nkt && ok; ++jt) {
+        const int f = t_glob + jt;
+        const int s = f & 1;
+        ok = warp_wait(&v_full[s], (f >> 1) & 1, p.err, abort_flag);
+        if (ok && f >= 1) ok = warp_wait(pv_done, (f - 1) & 1, p.err, abort_flag);  // V^T buffer free
+        if (!ok) break;
+        const uint32_t vbase = sb + C::OFF_V + s * C::kKVBytes;
+        const uint32_t tbase = sb + C::OFF_VT;
+        constexpr int DG = D / 32;  // groups of four 8-dim chunks
+        for (int o = tw; o < 16 * DG; o += 2) {
+          const int kb = o / DG;  // 8-key block
+          const int dg = o - kb * DG;
+          const int i = lane >> 3;
+          const int dc = 4 * dg + i;  // 8-dim chunk of this lane's source row
+          const int kr = 8 * kb + (lane & 7);
+          uint32_t r[4];
+          ldsm_x4_t_tc(r, vbase + (dc >> 3) * C::kBlk + box_off(kr, dc & 7));
+          const int key = jt * C::BK + 8 * kb + 2 * (lane & 3);
+          const uint32_t keep = (key < kv_end ? 0x0000ffffu : 0u) | (key + 1 < kv_end ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) r[x] &= keep;
+          const int dr = 8 * dc + (lane & 7);  // V^T row = head dim
+          stsm_x4(tbase + (kb >> 3) * (D * 128) + box_off(dr, kb & 7), r);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&v_empty[s]);
+          mbar_arrive(vt_full);
+        }
+      }
+    } else {
+      // -------------------------------------------------------------------- softmax
+      const int sw = warp - 4;  // TMEM lanes 32*sw .. 32*sw+31
+      const int r = 32 * sw + lane;
+      const bool live = r < qrows;
+      const int pos = pos0 + r;
+      const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sw) << 16);
+      float m_run = NEG_INF, l_run = 0.f;
+      bool ok = !*abort_flag;
+      for (int jt = 0; jt < nkt && ok; ++jt) {
+        const int f = t_glob + jt;
+        const int s = f & 1;
+        ok = warp_wait(&s_full[s], (f >> 1) & 1, p.err, abort_flag);
+        if (!ok) break;
+        tc5::fence_after();
+        float sc[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tc5::ld32(trow + 128u * s + 32u * c, v);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) sc[32 * c + x] = v[x];
+        }
+        tc5::wait_ld();
+        tc5::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[s]);
+        float mx = NEG_INF;
+        const int key0 = jt * C::BK;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          sc[c] = (live && key0 + c <= pos) ? sc[c] * p.qscale : NEG_INF;
+          mx = fmaxf(mx, sc[c]);
+        }
+        float corr = 1.f;
+        bool resc = false;
+        if (m_run == NEG_INF) {
+          m_run = mx;  // nothing accumulated for this row yet
+        } else if (mx > m_run + 8.f) {
+          corr = fast_exp2(m_run - mx);
+          m_run = mx;
+          resc = true;
+        }
+        const float base = m_run == NEG_INF ? 0.f : m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          sc[c] = fast_exp2(sc[c] - base);
+          lsum += sc[c];
+        }
+        l_run = l_run * corr + lsum;
+        if (jt > 0) {
+          ok = warp_wait(pv_done, (f - 1) & 1, p.err, abort_flag);  // P buffer free, O stable
+          if (!ok) break;
+          tc5::fence_after();
+          if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tc5::ld32(trow + C::COL_O + 32u * c, o);
+              tc5::wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] *= corr;
+              tc5::st32(trow + C::COL_O + 32u * c, o);
+            }
+            tc5::wait_st();
+          }
+        }
+        unsigned char* prow = smem + C::OFF_P + r * 128;
+#pragma unroll
+        for (int c16 = 0; c16 < 16; ++c16) {
+          uint4 u;
+          u.x = pack_bf16x2(sc[8 * c16 + 0], sc[8 * c16 + 1]);
+          u.y = pack_bf16x2(sc[8 * c16 + 2], sc[8 * c16 + 3]);
+          u.z = pack_bf16x2(sc[8 * c16 + 4], sc[8 * c16 + 5]);
+          u.w = pack_bf16x2(sc[8 * c16 + 6], sc[8 * c16 + 7]);
+          *reinterpret_cast<uint4*>(prow + (c16 >> 3) * C::kBlk + (((c16 & 7) ^ (r & 7)) << 4)) = u;
+        }
+        fence_proxy_async_smem();
+        tc5::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      if (ok) ok = warp_wait(pv_done, (t_glob + nkt - 1) & 1, p.err, abort_flag);
+      if (ok) {
+        tc5::fence_after();
+        const float inv = live ? 1.f / l_run : 0.f;
+        bf16* orow = p.out + static_cast<int64_t>(s0 + q0 + r) * p.o_st + static_cast<int64_t>(hq) * p.o_sh;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tc5::ld32(trow + C::COL_O + 32u * c, o);
+          tc5::wait_ld();
+          if (live) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              uint4 u;
+              u.x = pack_bf16x2(o[8 * x + 0] * inv, o[8 * x + 1] * inv);
+              u.y = pack_bf16x2(o[8 * x + 2] * inv, o[8 * x + 3] * inv);
+              u.z = pack_bf16x2(o[8 * x + 4] * inv, o[8 * x + 5] * inv);
+              u.w = pack_bf16x2(o[8 * x + 6] * inv, o[8 * x + 7] * inv);
+              *reinterpret_cast<uint4*>(orow + 32 * c + 8 * x) = u;
+            }
+          }
+        }
+        tc5::fence_before();
+      }
+    }
+    t_glob += nkt;
+    ++item_no;
+    __syncthreads();  // the item's buffers (Q, S, O, P) are free for the next item
+  }
+
+  // teardown: no MMA may still be in flight when TMEM is released
+  if (warp == 1) {
+    if (lane == 0) {
+      tc5::commit(fin);
+      mbar_wait(fin, 0, p.err);  // bounded, and not skipped after an abort
+    }
+    __syncwarp();
+    tc5::fence_after();
+    tc5::dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace pkv

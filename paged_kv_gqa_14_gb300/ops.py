@@ -76,6 +76,50 @@ def kv_append(q, k, v, positions, slot_mapping, k_cache, v_cache, rope_theta, st
     _lib.check("pkv_kv_append", st)
 
 
+def kv_append_paged(q, k, v, block_tables, context_lens, query_start_loc, k_cache, v_cache, rope_theta,
+                    positions_out=None, slot_mapping_out=None, max_blocks_per_seq=None, stream=None):
+    """kv_append with positions and slots derived on the GPU from the scheduler's tables
+    (``pkv_kv_append_paged``).  q is rotated in place."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _contig1(context_lens, "context_lens")
+    _contig1(query_start_loc, "query_start_loc")
+    if block_tables.stride(1) != 1:
+        raise ValueError("block_tables rows must be contiguous")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, 16, Hkv, d]")
+    T, hq, d = q.shape
+    nb, bs, hkv, dc = k_cache.shape
+    if k.shape != (T, hkv, d) or v.shape != (T, hkv, d) or dc != d or v_cache.shape != k_cache.shape:
+        raise ValueError("k / v / cache shapes disagree with q")
+    B = context_lens.shape[0]
+    if query_start_loc.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("query_start_loc must have num_seqs + 1 entries, block_tables num_seqs rows")
+    for name, t in (("positions_out", positions_out), ("slot_mapping_out", slot_mapping_out)):
+        if t is not None:
+            _need(t, name, torch.int64, 1)
+            _contig1(t, name)
+            if t.shape[0] != T:
+                raise ValueError(f"{name} must have num_tokens entries")
+    mb = block_tables.shape[1] if max_blocks_per_seq is None else int(max_blocks_per_seq)
+    qs, qh = _rows(q, "q")
+    ks, kh = _rows(k, "k")
+    vs, vh = _rows(v, "v")
+    st = _lib.load().pkv_kv_append_paged(
+        q.data_ptr(), qs, qh, k.data_ptr(), ks, kh, v.data_ptr(), vs, vh, block_tables.data_ptr(),
+        block_tables.stride(0), mb, context_lens.data_ptr(), query_start_loc.data_ptr(), B, k_cache.data_ptr(),
+        v_cache.data_ptr(), T, hq, hkv, d, nb, bs, float(rope_theta),
+        None if positions_out is None else positions_out.data_ptr(),
+        None if slot_mapping_out is None else slot_mapping_out.data_ptr(), _stream_ptr(stream))
+    _lib.check("pkv_kv_append_paged", st)
+
+
 def workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq):
     """Bytes of workspace ``paged_attention`` needs (``pkv_paged_attention_workspace_size``)."""
     n = _lib.load().pkv_paged_attention_workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads,
@@ -144,6 +188,14 @@ DECODE_KERNELS = {"auto": 0, "simt": 1, "tensor": 2}
 def set_decode_kernel(kind):
     """Decode arithmetic for later calls: "auto", "simt" (CUDA cores) or "tensor" (mma.sync)."""
     _lib.check("pkv_set_decode_kernel", _lib.load().pkv_set_decode_kernel(DECODE_KERNELS[kind]))
+
+
+PREFILL_KERNELS = {"auto": 0, "mma": 1, "tcgen05": 2}
+
+
+def set_prefill_kernel(kind):
+    """Prefill-tile arithmetic for later calls: "auto", "mma" (mma.sync) or "tcgen05"."""
+    _lib.check("pkv_set_prefill_kernel", _lib.load().pkv_set_prefill_kernel(PREFILL_KERNELS[kind]))
 
 
 def get_device_error(clear=True, stream=None):

@@ -89,6 +89,49 @@ def test_append_position_zero_is_exact_copy():
     assert np.array_equal(dev_to_bits(d.q), bt.q)
 
 
+@pytest.mark.parametrize("index", [1, 3, 5])
+def test_append_with_device_side_slots_matches_explicit_slots(index):
+    # positions and slots derived on the GPU from the tables equal the scheduler's, and the
+    # caches and q come out bit-identical to the explicit-slot call
+    bt = W.config(index)
+    ref = Dev(bt)
+    ref.append()
+    d = Dev(bt)
+    pos = torch.full((bt.num_tokens,), -7, dtype=torch.int64, device="cuda")
+    slots = torch.full((bt.num_tokens,), -7, dtype=torch.int64, device="cuda")
+    ops.kv_append_paged(d.q, d.k, d.v, d.block_tables, d.context_lens, d.qsl, d.k_cache, d.v_cache,
+                        bt.rope_theta, positions_out=pos, slot_mapping_out=slots)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    assert np.array_equal(pos.cpu().numpy(), bt.positions)
+    assert np.array_equal(slots.cpu().numpy(), bt.slot_mapping)
+    for a, b in ((d.k_cache, ref.k_cache), (d.v_cache, ref.v_cache), (d.q, ref.q)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_device_side_slots_skip_tokens_outside_spans():
+    bt = W.make_batch([20, 33, 5, 90], [3, 0, 5, 1], 8, 4, 64, 16, seed=14)
+    T = bt.num_tokens
+    # two extra trailing tokens that no span covers
+    q = np.concatenate([bt.q, bt.q[:2]])
+    k = np.concatenate([bt.k, bt.k[:2]])
+    v = np.concatenate([bt.v, bt.v[:2]])
+    d = Dev(bt)
+    d.q, d.k, d.v = bf16_to_dev(q), bf16_to_dev(k), bf16_to_dev(v)
+    pos = torch.zeros(T + 2, dtype=torch.int64, device="cuda")
+    slots = torch.zeros(T + 2, dtype=torch.int64, device="cuda")
+    ops.kv_append_paged(d.q, d.k, d.v, d.block_tables, d.context_lens, d.qsl, d.k_cache, d.v_cache,
+                        bt.rope_theta, positions_out=pos, slot_mapping_out=slots)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    assert np.array_equal(slots.cpu().numpy()[:T], bt.slot_mapping)
+    assert np.array_equal(pos.cpu().numpy()[:T], bt.positions)
+    assert np.all(slots.cpu().numpy()[T:] == -1)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
+                                     bt.rope_theta)
+    assert np.array_equal(dev_to_bits(d.v_cache), vc)
+
+
 def test_append_reads_strided_views_of_a_packed_qkv_buffer():
     bt = W.make_batch([17, 40, 3], [1, 1, 1], 16, 8, 128, 10, seed=4)
     T, hq, hkv, dd = bt.num_tokens, 16, 8, 128

@@ -83,6 +83,50 @@ def test_both_decode_kernels_random_shapes(seed, decode_kernel):
         assert_close(got, ref, f"{bt.name} decode={decode_kernel} ctas={ctas}")
 
 
+@pytest.fixture
+def prefill_kernel(request):
+    ops.set_prefill_kernel(request.param)
+    yield request.param
+    ops.set_prefill_kernel("auto")
+
+
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
+def test_both_prefill_kernels_on_mixed_workload(prefill_kernel):
+    bt, q_rot, kc, vc, ref = config_with_oracle(5)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert_close(got, ref, f"{bt.name} prefill={prefill_kernel}")
+
+
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
+@pytest.mark.parametrize("case", [
+    ([300, 40, 129], [300, 40, 129], 16, 8, 128),     # from-scratch chunks: ragged q tiles
+    ([1000, 700, 2], [260, 129, 2], 16, 8, 128),      # chunks over earlier context, tiny span
+    ([513, 64, 200], [257, 64, 1], 8, 8, 64),         # d 64, G 1, a decode row mixed in
+    ([900, 333], [200, 333], 28, 4, 128),             # G 7
+])
+def test_both_prefill_kernels_on_long_chunks(prefill_kernel, case):
+    ctx, spans, hq, hkv, d = case
+    pages = sum(-(-c // 16) for c in ctx)
+    bt = W.make_batch(ctx, spans, hq, hkv, d, pages + 5, seed=hash(tuple(ctx)) % 1000)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert_close(got, ref, f"prefill={prefill_kernel} ctx={ctx} spans={spans}")
+
+
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
+@pytest.mark.parametrize("seed", range(200, 210))
+def test_both_prefill_kernels_random_mixed(seed, prefill_kernel):
+    bt = W.random_case(seed, max_seqs=5, max_ctx=500, head_dims=(64, 128), groups=(1, 2, 4, 7),
+                       kv_heads=(1, 2, 4, 8))
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert_close(got, ref, f"{bt.name} prefill={prefill_kernel}")
+
+
 @pytest.mark.parametrize("ctas", [1, 7, 600])
 def test_split_count_does_not_change_the_result(ctas):
     bt, q_rot, kc, vc, ref = config_with_oracle(3)
