@@ -44,15 +44,16 @@ FALLBACK_HBM_GBS = 6800.0
 # ------------------------------------------------------------------------ workload facts
 def kv_unique_bytes(bt):
     """K+V bytes of every distinct (physical slot, kv head) the step's attention reads."""
+    bs = bt.block_size
     rows = set()
     for b in range(bt.num_seqs):
         n = int(bt.query_start_loc[b + 1] - bt.query_start_loc[b])
         if n == 0:
             continue
         ctx = int(bt.context_lens[b])
-        for j in range(-(-ctx // 16)):
+        for j in range(-(-ctx // bs)):
             blk = int(bt.block_tables[b, j])
-            last = min(16, ctx - 16 * j)
+            last = min(bs, ctx - bs * j)
             rows.update((blk, r) for r in range(last))
     return len(rows) * bt.num_kv_heads * bt.head_dim * 2 * 2
 
@@ -65,7 +66,7 @@ def kv_logical_bytes(bt):
 def decode_algorithmic_bytes(bt, kv_unique):
     """Algorithmic bytes of one decode-kernel launch: unique KV + q read + out write + tables."""
     qo = 2 * bt.num_tokens * bt.num_q_heads * bt.head_dim * 2
-    tables = int((-(-bt.context_lens.astype(np.int64) // 16)).sum()) * 4 + bt.num_seqs * 8
+    tables = int((-(-bt.context_lens.astype(np.int64) // bt.block_size)).sum()) * 4 + bt.num_seqs * 8
     return kv_unique + qo + tables
 
 
@@ -84,7 +85,8 @@ def sub_batch(bt, seqs):
     rows = np.array(rows, dtype=np.int64)
     tables = np.array([[remap[int(x)] if x >= 0 else -1 for x in bt.block_tables[b]] for b in seqs], dtype=np.int32)
     slots = bt.slot_mapping[rows]
-    new_slots = np.array([remap[int(s) // 16] * 16 + int(s) % 16 if s >= 0 else -1 for s in slots], dtype=np.int64)
+    bs = bt.block_size
+    new_slots = np.array([remap[int(s) // bs] * bs + int(s) % bs if s >= 0 else -1 for s in slots], dtype=np.int64)
     return W.Batch(name=bt.name + f"-sample{len(seqs)}", q=bt.q[rows], k=bt.k[rows], v=bt.v[rows],
                    positions=bt.positions[rows], slot_mapping=new_slots, k_cache=bt.k_cache[idx],
                    v_cache=bt.v_cache[idx], block_tables=tables, context_lens=bt.context_lens[seqs],
@@ -222,7 +224,7 @@ def run_gpu(args, rank, world, local_rank):
 
         dist.init_process_group("nccl", device_id=dev)
 
-    bt = W.config(args.workload, poison=False)
+    bt = W.config(args.workload, poison=False, block_size=args.block_size)
     if args.seqs:
         bt = sub_batch(bt, range(min(args.seqs, bt.num_seqs)))
     kv_u = kv_unique_bytes(bt)
@@ -376,7 +378,7 @@ def run_gpu(args, rank, world, local_rank):
             "num_q_heads": bt.num_q_heads,
             "num_kv_heads": bt.num_kv_heads,
             "head_dim": bt.head_dim,
-            "block_size": 16,
+            "block_size": bt.block_size,
             "context_lens": [int(bt.context_lens.min()), int(bt.context_lens.max())],
             "num_blocks": bt.num_blocks,
             "new_tokens": bt.num_tokens,
@@ -441,7 +443,7 @@ def run_gpu(args, rank, world, local_rank):
 
 # ----------------------------------------------------------------------- reference arm
 def run_reference(args):
-    bt = W.config(args.workload, poison=False)
+    bt = W.config(args.workload, poison=False, block_size=args.block_size)
     sb, dt, n = time_oracle(bt, budget_s=min(args.cpu_budget, 8.0))
     kv_s = kv_unique_bytes(sb)
     for _ in range(args.warmup):
@@ -486,6 +488,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32, 64, 128],
+                    help="tokens per pool block (the workload keeps its pool size in tokens)")
     ap.add_argument("--seqs", type=int, default=0, help="only the first N sequences (small profiling case)")
     ap.add_argument("--decode-kernel", choices=["auto", "simt", "tensor"], default="auto")
     ap.add_argument("--prefill-kernel", choices=["auto", "mma", "tcgen05"], default="auto")

@@ -7,7 +7,9 @@
  *   pkv_kv_append        fused RoPE + KV-cache write of the step's new tokens
  *                        ("mini_engine" README, "Next: fused kernels": fused RoPE, fused QKV
  *                        split and KV-cache write; "09 -- Mini Inference Engine (The
- *                        Capstone)", "Week 4 -- Paged KV cache": pool of 16-token blocks).
+ *                        Capstone)", "Week 4 -- Paged KV cache": pool of fixed-size
+ *                        blocks; "Design decisions you'll face": 16 tokens per block for
+ *                        a first engine, the block size a tunable to measure later).
  *   pkv_paged_attention  grouped-query attention of every new token over its sequence's
  *                        paged context, decode tokens and causal prefill chunks mixed in one
  *                        call ("mini_engine" README, "What it does": GQA, paged KV cache,
@@ -26,8 +28,10 @@
  *    other strides are in ELEMENTS.  Every row of head_dim elements must start on a 16-byte
  *    boundary (base pointers 16-byte aligned, strides multiples of 8 elements).
  *  - KV pool layout (per layer): k_cache and v_cache are each a contiguous bf16 tensor
- *    [num_blocks][block_size][num_kv_heads][head_dim] with block_size = 16.  Slot s denotes
- *    row (s % 16) of physical block (s / 16).
+ *    [num_blocks][block_size][num_kv_heads][head_dim].  block_size is a power of two from 8
+ *    to 128 (16 is the usual choice).  Slot s denotes row (s % block_size) of physical
+ *    block (s / block_size), i.e. row s of the pool viewed as
+ *    [num_blocks * block_size][num_kv_heads][head_dim].  num_blocks < 2^31 (int32 ids).
  *  - q head h attends with kv head h / (num_q_heads / num_kv_heads).
  *  - RoPE is the rotate-half form: pair (i, i + d/2) turns by pos * theta^(-2i/d).
  *  - Return value: PKV_OK, or a PKV_ERR_* code.  On a host-side validation error nothing is
@@ -65,15 +69,17 @@ extern "C" {
 #define PKV_ERR_CUDA 7        /* a CUDA runtime call or kernel launch failed                    */
 
 /* ---- device-side error bits (pkv_get_device_error) ---- */
-#define PKV_DEVERR_SLOT_RANGE 0x1u  /* kv_append: slot >= num_blocks*16; that write was skipped     */
+#define PKV_DEVERR_SLOT_RANGE 0x1u  /* kv_append: slot >= num_blocks*block_size; write skipped    */
 #define PKV_DEVERR_BLOCK_RANGE 0x2u /* attention: block id outside [0, num_blocks); read block 0  */
 #define PKV_DEVERR_SPAN 0x4u        /* attention: query_start_loc not monotone, past num_tokens,
                                        or context shorter than the span; sequence skipped        */
-#define PKV_DEVERR_CONTEXT 0x8u     /* attention: context > max_blocks_per_seq*16; seq skipped     */
+#define PKV_DEVERR_CONTEXT 0x8u     /* context > max_blocks_per_seq*block_size; seq/token skipped */
 #define PKV_DEVERR_TIMEOUT 0x10u    /* a bounded wait inside a kernel ran out; output unspecified */
 
-/* Supported sizes (compiled set). */
+/* Block sizes: the default, and the supported range (powers of two). */
 #define PKV_BLOCK_SIZE 16
+#define PKV_MIN_BLOCK_SIZE 8
+#define PKV_MAX_BLOCK_SIZE 128
 
 /* Human-readable name of a status code (static string, never NULL). */
 PKV_API const char* pkv_status_string(int status);
@@ -87,10 +93,11 @@ PKV_API int pkv_version(void);
  * For each new token t in [0, num_tokens):
  *   q[t, h, :]   <- bf16(rope(q[t, h, :], positions[t]))            for every q head (in place)
  *   if slot_mapping[t] >= 0, with s = slot_mapping[t]:
- *     k_cache[s/16, s%16, h, :] <- bf16(rope(k[t, h, :], positions[t]))   for every kv head
- *     v_cache[s/16, s%16, h, :] <- v[t, h, :]                              (bit copy)
+ *     k_cache[s/bs, s%bs, h, :] <- bf16(rope(k[t, h, :], positions[t]))   for every kv head
+ *     v_cache[s/bs, s%bs, h, :] <- v[t, h, :]                              (bit copy)
+ *   (bs = block_size)
  * Rotation: fp32 arithmetic on an angle reduced in fp64; rounding to bf16 nearest-even.
- * A negative slot marks padding and writes nothing.  A slot >= num_blocks*16 is skipped
+ * A negative slot marks padding and writes nothing.  A slot >= num_blocks*bs is skipped
  * and sets PKV_DEVERR_SLOT_RANGE.  Duplicate slots in one call give an unspecified row.
  *
  *   q_dev          bf16 [num_tokens][num_q_heads][head_dim], strides (q_stride_token,
@@ -99,7 +106,7 @@ PKV_API int pkv_version(void);
  *   positions_dev  int64 [num_tokens]: absolute position of each token (>= 0).
  *   slot_mapping_dev int64 [num_tokens]: destination slot, or < 0 to skip.
  *   k_cache_dev, v_cache_dev  bf16 pools (layout above) of num_blocks blocks.
- *   head_dim       64 or 128.   block_size  must be 16.
+ *   head_dim       64 or 128.   block_size  8, 16, 32, 64 or 128.
  *   rope_theta     RoPE base (> 0), e.g. 1e6 for Qwen3.
  * num_tokens == 0 is a no-op returning PKV_OK.
  */
@@ -118,7 +125,7 @@ PKV_API int pkv_kv_append(void* q_dev, int64_t q_stride_token, int64_t q_stride_
  * 7: GPU-side slot derivation).  Token t belongs to the sequence b whose span
  * [query_start_loc[b], query_start_loc[b+1]) contains it; it sits at position
  * pos = context_lens[b] - span_b + (t - query_start_loc[b]) and is written to slot
- * block_tables[b][pos / 16] * 16 + pos % 16.  Tokens outside every span are only rotated
+ * block_tables[b][pos / bs] * bs + pos % bs.  Tokens outside every span are only rotated
  * (q) and write nothing.  Inconsistent tables set PKV_DEVERR_SPAN / _CONTEXT / _BLOCK_RANGE
  * and skip the token's K/V write.  Table arguments as in pkv_paged_attention; the others as in
  * pkv_kv_append.  positions_out / slot_mapping_out (int64 [num_tokens], may be NULL) receive
@@ -151,7 +158,8 @@ PKV_API size_t pkv_paged_attention_workspace_size(int64_t num_tokens, int64_t nu
  *
  * Sequence b owns query rows [query_start_loc[b], query_start_loc[b+1]) (its span, n rows)
  * and context_lens[b] keys (ctx, counting the span's own tokens, which kv_append has already
- * written).  Its keys live in physical blocks block_tables[b, 0 .. ceil(ctx/16)-1].
+ * written).  Its keys live in physical blocks block_tables[b, 0 .. ceil(ctx/bs)-1]
+ * (bs = block_size).
  * Row r of the span is the token at position ctx - n + r; for every q head h:
  *     out[row, h, :] = softmax_j(scale * q[row, h, :] . K[j, h/G, :]) V[j, h/G, :],
  *     j over keys 0 .. ctx - n + r           (G = num_q_heads / num_kv_heads)
@@ -160,9 +168,10 @@ PKV_API size_t pkv_paged_attention_workspace_size(int64_t num_tokens, int64_t nu
  * Rows of out outside every span are not written.  Spans may be empty.
  *
  *   q_dev            bf16 [num_tokens][num_q_heads][head_dim] (already rotated), strides as given.
- *   k_cache_dev, v_cache_dev  the pool (layout above), num_blocks blocks of block_size 16.
+ *   k_cache_dev, v_cache_dev  the pool (layout above), num_blocks blocks of block_size
+ *                    tokens (8, 16, 32, 64 or 128).
  *   block_tables_dev int32 [num_seqs][block_tables_stride]; only the first
- *                    ceil(ctx/16) <= max_blocks_per_seq entries of row b are read.
+ *                    ceil(ctx/bs) <= max_blocks_per_seq entries of row b are read.
  *   context_lens_dev int32 [num_seqs].
  *   query_start_loc_dev int32 [num_seqs + 1], non-decreasing, [0] = 0, [num_seqs] <= num_tokens.
  *   out_dev          bf16 [num_tokens][num_q_heads][head_dim], strides as given; must not

@@ -141,7 +141,9 @@ int pkv_kv_append(void* q, int64_t q_st, int64_t q_sh, const void* k, int64_t k_
   if (num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0) return PKV_ERR_SHAPE;
   if (num_q_heads % num_kv_heads) return PKV_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  const int bs_log2 = block_size_log2(block_size);
+  if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
+  if (num_blocks > INT32_MAX) return PKV_ERR_SHAPE;  // block ids are int32
   if (!(rope_theta > 0.0)) return PKV_ERR_SHAPE;
   if (num_tokens == 0) return PKV_OK;
   if (!q || !k || !v || !positions || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_NULL;
@@ -167,7 +169,8 @@ int pkv_kv_append(void* q, int64_t q_st, int64_t q_sh, const void* k, int64_t k_
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.num_tokens = num_tokens;
-  a.num_slots = num_blocks * kBlockSize;
+  a.num_slots = num_blocks << bs_log2;
+  a.bs_log2 = bs_log2;
   a.hq = static_cast<int>(num_q_heads);
   a.hkv = static_cast<int>(num_kv_heads);
   a.head_dim = static_cast<int>(head_dim);
@@ -187,7 +190,9 @@ int pkv_kv_append_paged(void* q, int64_t q_st, int64_t q_sh, const void* k, int6
     return PKV_ERR_SHAPE;
   if (num_q_heads % num_kv_heads) return PKV_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  const int bs_log2 = block_size_log2(block_size);
+  if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
+  if (num_blocks > INT32_MAX) return PKV_ERR_SHAPE;  // block ids are int32
   if (!(rope_theta > 0.0)) return PKV_ERR_SHAPE;
   if (num_seqs > (1 << 30)) return PKV_ERR_SHAPE;
   if (num_tokens == 0) return PKV_OK;
@@ -222,7 +227,8 @@ int pkv_kv_append_paged(void* q, int64_t q_st, int64_t q_sh, const void* k, int6
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.num_tokens = num_tokens;
-  a.num_slots = num_blocks * kBlockSize;
+  a.num_slots = num_blocks << bs_log2;
+  a.bs_log2 = bs_log2;
   a.hq = static_cast<int>(num_q_heads);
   a.hkv = static_cast<int>(num_kv_heads);
   a.head_dim = static_cast<int>(head_dim);
@@ -254,7 +260,9 @@ int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k
     return PKV_ERR_SHAPE;
   if (num_q_heads % num_kv_heads) return PKV_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  const int bs_log2 = block_size_log2(block_size);
+  if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
+  if (num_blocks > INT32_MAX) return PKV_ERR_SHAPE;  // block ids are int32
   if (kDecodeWarps % num_kv_heads) return PKV_ERR_UNSUPPORTED;
   const int64_t group = num_q_heads / num_kv_heads;
   if (group < 1 || group > 8) return PKV_ERR_UNSUPPORTED;
@@ -280,6 +288,7 @@ int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.num_blocks = num_blocks;
+  a.bs_log2 = bs_log2;
   a.block_tables = block_tables;
   a.bt_stride = bt_stride;
   a.max_blocks = max_blocks_per_seq;

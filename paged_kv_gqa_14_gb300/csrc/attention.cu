@@ -81,7 +81,7 @@ __device__ Int3 block_scan3(Int3 v, Int3& tot, int* sm /* [3 * 32] */) {
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ qsl,
                                                             const int32_t* __restrict__ ctxl,
                                                             int num_seqs, int64_t num_tokens,
-                                                            int64_t max_blocks, int pps,
+                                                            int64_t max_ctx, int pps,
                                                             int decode_ctas, int tile_q, Plan plan,
                                                             int64_t max_tiles, unsigned int* err) {
   __shared__ int sm[3 * 32];
@@ -104,14 +104,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         if (ctx < span) {
           raise_error(err, PKV_DEVERR_SPAN);
           ok = false;
-        } else if (static_cast<int64_t>(ctx) > max_blocks * kBlockSize) {
+        } else if (static_cast<int64_t>(ctx) > max_ctx) {  // more keys than the table row maps
           raise_error(err, PKV_DEVERR_CONTEXT);
           ok = false;
         }
       }
       if (ok && span == 1) {
         v.a = 1;
-        v.b = ceil_div(ceil_div(ctx, kBlockSize), pps);
+        v.b = ceil_div(ceil_div(ctx, kPageTokens), pps);
       }
       if (ok && span > 1) v.c = ceil_div(span, tile_q);
     }
@@ -195,6 +195,7 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   p.k_cache = static_cast<const bf16*>(a.k_cache);
   p.v_cache = static_cast<const bf16*>(a.v_cache);
   p.num_blocks = a.num_blocks;
+  p.bs_log2 = a.bs_log2;
   p.block_tables = a.block_tables;
   p.bt_stride = a.bt_stride;
   p.context_lens = a.context_lens;
@@ -233,37 +234,39 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// The pool [num_blocks][16][Hkv][d] as a 4-D tensor {d, Hkv, 16, num_blocks}; a box is the
-// 16 token rows x 64 dims of one kv head in one block, 128-byte swizzled.
-bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D) {
+// The pool [num_blocks][block_size][Hkv][d] as a 4-D tensor {d, Hkv, block_size, num_blocks};
+// a box is min(block_size, 16) token rows x 64 dims of one kv head in one block, 128-byte
+// swizzled.
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv), 16,
+  const cuuint64_t bs = cuuint64_t(1) << bs_log2;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv), bs,
                               static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hkv) * D * 2,
-                                 static_cast<cuuint64_t>(16) * hkv * D * 2};
-  const cuuint32_t box[4] = {64, 1, 16, 1};
+                                 bs * hkv * D * 2};
+  const cuuint32_t box[4] = {64, 1, bs < 16 ? static_cast<cuuint32_t>(bs) : 16u, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G>
+template <int D, int G, int BS>
 cudaError_t launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
   using C = DecodeTcCfg<D, G>;
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   DecodeTcParams P;
-  if (!make_pool_map(&P.tmap_k, a.k_cache, a.num_blocks, a.hkv, D) ||
-      !make_pool_map(&P.tmap_v, a.v_cache, a.num_blocks, a.hkv, D))
+  if (!make_pool_map(&P.tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, D) ||
+      !make_pool_map(&P.tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, D))
     return cudaErrorInvalidValue;
   DecodeParams& p = P.p;
   p.q = static_cast<const bf16*>(a.q);
@@ -272,6 +275,7 @@ cudaError_t launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
   p.k_cache = static_cast<const bf16*>(a.k_cache);
   p.v_cache = static_cast<const bf16*>(a.v_cache);
   p.num_blocks = a.num_blocks;
+  p.bs_log2 = a.bs_log2;
   p.block_tables = a.block_tables;
   p.bt_stride = a.bt_stride;
   p.context_lens = a.context_lens;
@@ -285,7 +289,7 @@ cudaError_t launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
   p.plan = a.plan;
   p.err = a.err;
   record_kernel_event(PKV_KERNEL_DECODE, false, stream);
-  const cudaError_t e = launch_pdl(decode_tc_kernel<D, G>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
+  const cudaError_t e = launch_pdl(decode_tc_kernel<D, G, BS>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
                                    C::kSmemBytes, stream, P);
   record_kernel_event(PKV_KERNEL_DECODE, true, stream);
   return e;
@@ -294,7 +298,9 @@ cudaError_t launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
 template <int D, int G>
 cudaError_t launch_decode_pick(const AttnArgs& a, cudaStream_t stream) {
   const int kind = a.decode_kernel != 0 ? a.decode_kernel : (G >= kTensorDecodeMinGroup ? 2 : 1);
-  return kind == 2 ? launch_decode_tc<D, G>(a, stream) : launch_decode<D, G>(a, stream);
+  if (kind != 2) return launch_decode<D, G>(a, stream);
+  // 16-token blocks get the instance with the block size folded in
+  return a.bs_log2 == 4 ? launch_decode_tc<D, G, 16>(a, stream) : launch_decode_tc<D, G, 0>(a, stream);
 }
 
 template <int D>
@@ -328,8 +334,9 @@ bool make_q_map(CUtensorMap* m, const AttnArgs& a) {
 
 bool make_prefill_tc_params(const AttnArgs& a, PrefillTcParams* P) {
   if (a.q_sh <= 0 || a.q_st <= 0) return false;
-  if (!make_q_map(&P->tmap_q, a) || !make_pool_map(&P->tmap_k, a.k_cache, a.num_blocks, a.hkv, a.head_dim) ||
-      !make_pool_map(&P->tmap_v, a.v_cache, a.num_blocks, a.hkv, a.head_dim))
+  if (!make_q_map(&P->tmap_q, a) ||
+      !make_pool_map(&P->tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, a.head_dim) ||
+      !make_pool_map(&P->tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, a.head_dim))
     return false;
   P->p = make_prefill_params(a);
   return true;
@@ -368,7 +375,8 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   const int tile_q = use_tc ? PrefillTcCfg<128>::BQ : kPrefillTileQ;
   record_kernel_event(PKV_KERNEL_PLAN, false, stream);
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
-                             static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks, pps, a.decode_ctas, tile_q,
+                             static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps,
+                             a.decode_ctas, tile_q,
                              a.plan, a.max_tiles, a.err);
   record_kernel_event(PKV_KERNEL_PLAN, true, stream);
   if (e != cudaSuccess) return e;

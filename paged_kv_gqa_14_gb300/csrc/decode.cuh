@@ -32,6 +32,7 @@ struct DecodeParams {
   const bf16* k_cache;
   const bf16* v_cache;
   int64_t num_blocks;
+  int bs_log2;  // log2 of the pool's block size
   const int32_t* block_tables;
   int64_t bt_stride;
   const int32_t* context_lens;
@@ -218,7 +219,12 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     int i = i_first;
     int ustart = dec_unit[i], unext = dec_unit[i + 1];
     int b = p.plan.dec_seq[i];
-    int npages = ceil_div(p.context_lens[b], 16);
+    int ctx = p.context_lens[b];
+    int npages = ceil_div(ctx, 16);
+    const int sh = p.bs_log2;
+    const int bmask = (1 << sh) - 1;
+    const int piece_rows = sh >= 4 ? 16 : 8;  // rows of one contiguous copy
+    const int64_t row_elems = static_cast<int64_t>(hkv) * D;
     int it = 0;
     for (int u = ubeg; u < uend; ++u, ++it) {
       while (u >= unext) {
@@ -226,30 +232,36 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
         ustart = unext;
         unext = dec_unit[i + 1];
         b = p.plan.dec_seq[i];
-        npages = ceil_div(p.context_lens[b], 16);
+        ctx = p.context_lens[b];
+        npages = ceil_div(ctx, 16);
       }
       const int pg0 = (u - ustart) * pps;
       const int npg = min(pps, npages - pg0);
       const int s = it % STAGES;
       if (it >= STAGES && !wait_or_abort(&empty[s], ((it / STAGES) - 1) & 1, p.err, abort_flag)) break;
-      // block ids of this unit's pages (lanes < npg: K, lanes npg..2npg-1: V)
-      const int which = lane >= npg ? 1 : 0;
-      const int pg = lane - which * npg;
-      int blk = 0;
-      if (lane < 2 * npg) {
-        blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + pg0 + pg];
-        if (blk < 0 || blk >= p.num_blocks) {
-          raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
-          blk = 0;
-        }
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * npg * page_bytes);
+      // with 8-token blocks the last page's second half is not copied when it lies past the
+      // context (its block may not exist); the consumers never read those rows
+      const bool tail_half = piece_rows == 8 && (pg0 + npg - 1) * 16 + 8 >= ctx;
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * (npg * page_bytes - (tail_half ? page_bytes / 2 : 0u)));
       __syncwarp();
+      // lanes < npg copy K pages, lanes npg..2npg-1 the V pages
       if (lane < 2 * npg) {
-        const bf16* src = (which ? p.v_cache : p.k_cache) + static_cast<int64_t>(blk) * page_elems;
+        const int which = lane >= npg ? 1 : 0;
+        const int pg = lane - which * npg;
+        const int tok = (pg0 + pg) * 16;
         bf16* dst = stages + static_cast<int64_t>(s) * 2 * C::kStageElems + which * C::kStageElems +
                     pg * page_elems;
-        bulk_g2s(dst, src, page_bytes, &full[s], pol);
+        for (int r = 0; r < 16 && tok + r < ctx; r += piece_rows) {
+          const int tr = tok + r;
+          int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (tr >> sh)];
+          if (blk < 0 || blk >= p.num_blocks) {
+            raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+            blk = 0;
+          }
+          const bf16* src = (which ? p.v_cache : p.k_cache) +
+                            ((static_cast<int64_t>(blk) << sh) + (tr & bmask)) * row_elems;
+          bulk_g2s(dst + r * row_elems, src, page_bytes / (16 / piece_rows), &full[s], pol);
+        }
       }
     }
     // do not leave while this warp's copies may still be landing: the last fill of each

@@ -15,8 +15,17 @@
 // loaded element plus shuffle reductions) that caps the scalar kernel at large G.
 //
 // K/V pages are staged by 4-D TMA tensor loads (tensor map over the pool viewed as
-// [num_blocks][16][Hkv][d]) in boxes of 16 tokens x 64 dims of one kv head with the 128-byte
-// swizzle, so the ldmatrix reads of 8 token rows hit 8 different bank groups.
+// [num_blocks][block_size][Hkv][d]) in boxes of 16 tokens x 64 dims of one kv head with the
+// 128-byte swizzle, so the ldmatrix reads of 8 token rows hit 8 different bank groups.  A
+// 16-token page is rows 16j..16j+15 of one block when blocks hold 16 or more tokens; with
+// 8-token blocks it is two boxes of 8 rows from two blocks, landing 1024 bytes apart, which
+// with the 128-byte swizzle is the same shared-memory image as one 16-row box.
+//
+// The producer is instantiated twice: for 16-token blocks (the default pool) with the block
+// size folded in at compile time, and for every other block size with it read at run time.
+// The kernel is sensitive to the producer warp's instruction stream (it shares a scheduler
+// with two consumer warps and sits on the ring's refill path): on GB300 the run-time form
+// costs about 8% of decode time at 16-token blocks, the compile-time form nothing.
 #pragma once
 
 #include <cuda.h>
@@ -26,7 +35,7 @@
 namespace pkv {
 
 struct DecodeTcParams {
-  CUtensorMap tmap_k;  // 4-D: {d, Hkv, 16, num_blocks}, box {64, 1, 16, 1}, 128B swizzle
+  CUtensorMap tmap_k;  // 4-D: {d, Hkv, block_size, num_blocks}, box {64, 1, min(block_size, 16), 1}, 128B swizzle
   CUtensorMap tmap_v;
   DecodeParams p;
 };
@@ -87,7 +96,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // byte offset of 16-byte chunk `c` (0..7) of token row `t` inside a 128B-swizzled box
 __device__ __forceinline__ uint32_t box_off(int t, int c) { return t * 128 + ((c ^ (t & 7)) << 4); }
 
-template <int D, int G>
+// BS: 16 for pools of 16-token blocks, 0 for any other block size (read from the params).
+template <int D, int G, int BS>
 __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams P) {
   using C = DecodeTcCfg<D, G>;
@@ -160,7 +170,13 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     int i = i_first;
     int ustart = dec_unit[i], unext = dec_unit[i + 1];
     int b = p.plan.dec_seq[i];
-    int npages = ceil_div(p.context_lens[b], 16);
+    int ctx = p.context_lens[b];
+    int npages = ceil_div(ctx, 16);
+    // page gp: block gp >> s4 and its rows from (16 gp) & bmask when blocks hold 16 << s4
+    // tokens; blocks 2 gp and 2 gp + 1 (the second only if it holds context) when they hold 8
+    const int sh = BS == 16 ? 4 : p.bs_log2;
+    const int bmask = (1 << sh) - 1;
+    const bool two_blocks = BS == 16 ? false : sh == 3;
     int it = 0;
     for (int u = ubeg; u < uend; ++u, ++it) {
       while (u >= unext) {
@@ -168,27 +184,41 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
         ustart = unext;
         unext = dec_unit[i + 1];
         b = p.plan.dec_seq[i];
-        npages = ceil_div(p.context_lens[b], 16);
+        ctx = p.context_lens[b];
+        npages = ceil_div(ctx, 16);
       }
       const int pg0 = (u - ustart) * pps;
       const int npg = min(pps, npages - pg0);
       const int s = it % STAGES;
       if (it >= STAGES && !wait_or_abort(&empty[s], ((it / STAGES) - 1) & 1, p.err, abort_flag)) break;
-      int blk = 0;
+      int blk = 0, blk2 = -1;
       const bool issue = lane_has_box && bp < npg;
+      const int gp = pg0 + bp;
       if (issue) {
-        blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + pg0 + bp];
+        const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
+        blk = row[two_blocks ? 2 * gp : gp >> (sh - 4)];
         if (blk < 0 || blk >= p.num_blocks) {
           raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
           blk = 0;
         }
+        if (two_blocks && gp * 16 + 8 < ctx) {
+          blk2 = row[2 * gp + 1];
+          if (blk2 < 0 || blk2 >= p.num_blocks) {
+            raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+            blk2 = 0;
+          }
+        }
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * npg * page_bytes);
+      // a last half page past the context is not loaded (8-token blocks)
+      const bool tail_half = two_blocks && (pg0 + npg - 1) * 16 + 8 >= ctx;
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * (npg * page_bytes - (tail_half ? page_bytes / 2 : 0u)));
       __syncwarp();
       if (issue) {
         unsigned char* dst = stages + s * C::kStageBytes + kv * C::kPartBytes +
                              ((bp * hkv + bh) * HALVES + bhalf) * C::kBoxBytes;
-        tma_load_4d(dst, kv ? &P.tmap_v : &P.tmap_k, bhalf * 64, bh, 0, blk, &full[s], pol);
+        const CUtensorMap* map = kv ? &P.tmap_v : &P.tmap_k;
+        tma_load_4d(dst, map, bhalf * 64, bh, (gp * 16) & bmask, blk, &full[s], pol);
+        if (blk2 >= 0) tma_load_4d(dst + 1024, map, bhalf * 64, bh, 0, blk2, &full[s], pol);
       }
     }
     const int issued = it;

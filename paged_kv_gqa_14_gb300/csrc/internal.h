@@ -7,7 +7,18 @@
 
 namespace pkv {
 
-constexpr int kBlockSize = 16;       // tokens per KV block (the pool's block_size)
+// The kernels walk a sequence's keys in pages of 16 tokens whatever the pool's block size:
+// the pool's blocks hold 2^k tokens, 8 <= 2^k <= 128, so a page is a 16-row piece of one
+// block (block_size >= 16) or two whole blocks (block_size 8).
+constexpr int kPageTokens = 16;
+constexpr int kMinBlockSize = 8;
+constexpr int kMaxBlockSize = 128;
+// log2(block_size) for a supported block size, else -1.
+inline int block_size_log2(int64_t bs) {
+  for (int l = 3; (1 << l) <= kMaxBlockSize; ++l)
+    if (bs == (int64_t(1) << l)) return l;
+  return -1;
+}
 constexpr int kDecodeWarps = 8;      // consumer warps of the decode split-K kernel
 constexpr int kPrefillTileQ = 64;    // query rows per prefill work tile
 constexpr int kMaxHeadDim = 128;
@@ -27,7 +38,7 @@ constexpr int kTensorDecodeMinGroup = 1;
 // header[4] partial-result slots in use                        S
 //
 // A decode work unit is one page group of one sequence: P = kDecodeWarps / Hkv
-// consecutive 16-token pages, all kv heads.  Decode CTA c owns units [c W, (c+1) W) of
+// consecutive 16-token pages (kPageTokens), all kv heads.  Decode CTA c owns units [c W, (c+1) W) of
 // the concatenation of all decode sequences' units.
 struct Plan {
   int* header;      // [16]
@@ -72,6 +83,7 @@ struct AppendArgs {
   void* k_cache;
   void* v_cache;
   int64_t num_tokens, num_slots;
+  int bs_log2;  // log2 of the pool's block size
   int hq, hkv, head_dim;
   double theta;
   unsigned int* err;
@@ -84,6 +96,7 @@ struct AttnArgs {
   const void* k_cache;
   const void* v_cache;
   int64_t num_blocks;
+  int bs_log2;  // log2 of the pool's block size
   const int32_t* block_tables;
   int64_t bt_stride, max_blocks;
   const int32_t* context_lens;

@@ -1,6 +1,7 @@
 // Fused RoPE + KV-cache append ("mini_engine" README, "Next: fused kernels": fused RoPE
 // and fused QKV split + KV-cache write; "09 -- Mini Inference Engine (The Capstone)",
-// "Week 4 -- Paged KV cache": pool of 16-token blocks addressed by slot).
+// "Week 4 -- Paged KV cache": pool of fixed-size blocks addressed by slot; the block size is
+// 16 by default and any power of two from 8 to 128 here).
 //
 // One CTA per new token.  The token's d/2 rotation angles are computed once into shared
 // memory: angle = pos * f_i with f_i = theta^(-2i/d) (fp64 on the host), reduced to
@@ -26,6 +27,7 @@ struct AppendSrc {
   const int32_t* ctxl;
   const int32_t* bt;
   int64_t bt_stride, max_blocks, num_seqs;
+  int bs_log2;  // log2 of the pool's block size
   int64_t* pos_out;
   int64_t* slot_out;
 };
@@ -54,7 +56,7 @@ __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float2* cs) 
 // Position and slot of token t, derived on the device from the scheduler's tables: the
 // token's sequence b is the last one with query_start_loc[b] <= t (found by a warp-wide
 // search, 32 samples per round), it sits at position ctx_b - n_b + (t - qsl[b]) and its slot
-// is row pos % 16 of block block_tables[b][pos / 16].  Tokens outside every span get slot -1.
+// is row pos % bs of block block_tables[b][pos / bs].  Tokens outside every span get slot -1.
 __device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t num_blocks, unsigned int* err,
                             int64_t& pos, int64_t& slot) {
   const int32_t* qsl = src.qsl;
@@ -69,8 +71,8 @@ __device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t n
       break;
     }
     const int stride = (len + 31) / 32;
-    const int idx = min(lo + lane * stride, hi);
-    const unsigned m = __ballot_sync(0xffffffffu, qsl[idx] <= t);
+    const int idx = lo + lane * stride;  // samples past hi take no part in the count
+    const unsigned m = __ballot_sync(0xffffffffu, idx <= hi && qsl[idx] <= t);
     const int k = __popc(m) - 1;
     if (k < 0) break;
     const int nlo = lo + k * stride;
@@ -89,7 +91,7 @@ __device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t n
     return;
   }
   pos = static_cast<int64_t>(ctx) - n + (t - s0);
-  const int64_t page = pos / 16;
+  const int64_t page = pos >> src.bs_log2;
   if (page >= src.max_blocks) {
     if (lane == 0) raise_error(err, PKV_DEVERR_CONTEXT);
     return;
@@ -99,7 +101,7 @@ __device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t n
     if (lane == 0) raise_error(err, PKV_DEVERR_BLOCK_RANGE);
     return;
   }
-  slot = static_cast<int64_t>(blk) * 16 + pos % 16;
+  slot = (static_cast<int64_t>(blk) << src.bs_log2) + (pos & ((int64_t(1) << src.bs_log2) - 1));
 }
 
 template <int D>
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
   if (threadIdx.x < 32) {
     int64_t p_, s_;
     if (src.qsl) {
-      derive_slot(src, t, threadIdx.x, num_slots / 16, err, p_, s_);
+      derive_slot(src, t, threadIdx.x, num_slots >> src.bs_log2, err, p_, s_);
     } else {
       p_ = src.positions[t];
       s_ = src.slots[t];
@@ -201,6 +203,7 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   src.bt_stride = a.bt_stride;
   src.max_blocks = a.max_blocks;
   src.num_seqs = a.num_seqs;
+  src.bs_log2 = a.bs_log2;
   src.pos_out = a.positions_out;
   src.slot_out = a.slots_out;
   record_kernel_event(PKV_KERNEL_APPEND, false, stream);

@@ -23,6 +23,7 @@ struct PrefillParams {
   const bf16* k_cache;
   const bf16* v_cache;
   int64_t num_blocks;
+  int bs_log2;  // log2 of the pool's block size
   const int32_t* block_tables;
   int64_t bt_stride;
   const int32_t* context_lens;
@@ -108,13 +109,14 @@ __device__ __forceinline__ void load_kv_tile(bf16* sK, bf16* sV, const PrefillPa
     const bool valid = key < kv_end;
     int blk = 0;
     if (valid) {
-      blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (key >> 4)];
+      blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (key >> p.bs_log2)];
       if (blk < 0 || blk >= p.num_blocks) {
         raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
         blk = 0;
       }
     }
-    const int64_t off = (static_cast<int64_t>(blk) * 16 + (key & 15)) * row_elems + h * D + ch * 8;
+    const int64_t off =
+        ((static_cast<int64_t>(blk) << p.bs_log2) + (key & ((1 << p.bs_log2) - 1))) * row_elems + h * D + ch * 8;
     cp_async16(sK + swz<C::CH>(r, ch) * 8, p.k_cache + (valid ? off : 0), valid);
     cp_async16(sV + swz<C::CH>(r, ch) * 8, p.v_cache + (valid ? off : 0), valid);
   }
@@ -301,6 +303,7 @@ inline PrefillParams make_prefill_params(const AttnArgs& a) {
   p.k_cache = static_cast<const bf16*>(a.k_cache);
   p.v_cache = static_cast<const bf16*>(a.v_cache);
   p.num_blocks = a.num_blocks;
+  p.bs_log2 = a.bs_log2;
   p.block_tables = a.block_tables;
   p.bt_stride = a.bt_stride;
   p.context_lens = a.context_lens;

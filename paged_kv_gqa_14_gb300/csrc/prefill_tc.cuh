@@ -132,6 +132,14 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_v)) : "memory");
   }
+  pdl_wait();  // the tile list is written by the planner kernel
+  pdl_trigger();
+  const int n_tiles = p.plan.header[3];
+  const int total = n_tiles * p.hq;
+  // A CTA whose first snake-order slot is past the item list has no item in any wave
+  // (every later slot is at least gridDim.x): it leaves before taking TMEM.  On a batch
+  // without prefill spans that is every CTA.
+  if (static_cast<int>(blockIdx.x) >= total) return;
   if (warp == 1) {
     tc5::alloc(tmem_slot, C::TMEM_COLS);
     tc5::relinquish();
@@ -140,11 +148,6 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   __syncthreads();
   tc5::fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  pdl_wait();  // the tile list is written by the planner kernel
-  pdl_trigger();
-  const int n_tiles = p.plan.header[3];
-  const int total = n_tiles * p.hq;
   const int G = p.hq / p.hkv;
   const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by the other items
 
@@ -177,7 +180,9 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
         __syncwarp();
         if (lane < HALVES) tma_load_3d(smem + C::OFF_Q + lane * C::kBlk, &P.tmap_q, lane * 64, hq, s0 + q0, q_full);
       }
-      const int per = 8 * HALVES;  // boxes per K (or V) tile
+      const int per = 8 * HALVES;  // 16-row boxes per K (or V) tile
+      const int bmask = (1 << p.bs_log2) - 1;
+      const int box_rows = p.bs_log2 >= 4 ? 16 : 8;  // the tensor map's box height
       const int kv = lane / per;
       const int rem = lane - kv * per;
       const int pg = rem / HALVES;
@@ -191,19 +196,29 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
           if (!ok) break;
         }
         const int npg = min(8, npages - jt * 8);
+        // 16-token pages: rows 16j..16j+15 of one block, or (8-token blocks) two boxes of 8
+        // rows from two blocks, 1024 bytes apart in shared memory; a last half past kv_end
+        // is not loaded (its block may not exist, and those keys are masked)
+        const bool tail_half = box_rows == 8 && jt * C::BK + (npg - 1) * 16 + 8 >= kv_end;
+        const uint32_t tile_bytes = static_cast<uint32_t>((npg * 2 - (tail_half ? 1 : 0)) * HALVES * 1024);
         if (lane == 0) {
-          mbar_arrive_expect_tx(&k_full[s], static_cast<uint32_t>(npg * HALVES * 2048));
-          mbar_arrive_expect_tx(&v_full[s], static_cast<uint32_t>(npg * HALVES * 2048));
+          mbar_arrive_expect_tx(&k_full[s], tile_bytes);
+          mbar_arrive_expect_tx(&v_full[s], tile_bytes);
         }
         __syncwarp();
         if (lane < 2 * per && pg < npg) {
-          int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + jt * 8 + pg];
-          if (blk < 0 || blk >= p.num_blocks) {
-            raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
-            blk = 0;
-          }
           unsigned char* dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::kKVBytes + half * C::kBlk + pg * 2048;
-          tma_load_4d(dst, kv ? &P.tmap_v : &P.tmap_k, half * 64, h, 0, blk, kv ? &v_full[s] : &k_full[s], pol);
+          const int tok = jt * C::BK + pg * 16;
+          for (int r = 0; r < 16 && tok + r < kv_end; r += box_rows) {
+            const int tr = tok + r;
+            int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (tr >> p.bs_log2)];
+            if (blk < 0 || blk >= p.num_blocks) {
+              raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+              blk = 0;
+            }
+            tma_load_4d(dst + r * 128, kv ? &P.tmap_v : &P.tmap_k, half * 64, h, tr & bmask, blk,
+                        kv ? &v_full[s] : &k_full[s], pol);
+          }
         }
       }
     } else if (warp == 1) {

@@ -14,7 +14,8 @@ import torch
 
 from . import _lib
 
-BLOCK_SIZE = 16
+BLOCK_SIZE = 16  # the pool's default block size
+SUPPORTED_BLOCK_SIZES = (8, 16, 32, 64, 128)
 
 
 def _stream_ptr(stream):
@@ -57,7 +58,7 @@ def kv_append(q, k, v, positions, slot_mapping, k_cache, v_cache, rope_theta, st
     _contig1(positions, "positions")
     _contig1(slot_mapping, "slot_mapping")
     if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
-        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, 16, Hkv, d]")
+        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, block_size, Hkv, d]")
     if k_cache.shape != v_cache.shape:
         raise ValueError("k_cache and v_cache differ in shape")
     T, hq, d = q.shape
@@ -93,7 +94,7 @@ def kv_append_paged(q, k, v, block_tables, context_lens, query_start_loc, k_cach
     if block_tables.stride(1) != 1:
         raise ValueError("block_tables rows must be contiguous")
     if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
-        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, 16, Hkv, d]")
+        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, block_size, Hkv, d]")
     T, hq, d = q.shape
     nb, bs, hkv, dc = k_cache.shape
     if k.shape != (T, hkv, d) or v.shape != (T, hkv, d) or dc != d or v_cache.shape != k_cache.shape:
@@ -150,7 +151,7 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, query_start
     if block_tables.stride(1) != 1:
         raise ValueError("block_tables rows must be contiguous")
     if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
-        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, 16, Hkv, d]")
+        raise ValueError("k_cache / v_cache must be contiguous [num_blocks, block_size, Hkv, d]")
     T, hq, d = q.shape
     nb, bs, hkv, dc = k_cache.shape
     if dc != d or v_cache.shape != k_cache.shape:

@@ -55,8 +55,8 @@ class Batch:
     v: np.ndarray  # uint16 [T, Hkv, d]
     positions: np.ndarray  # int64 [T]
     slot_mapping: np.ndarray  # int64 [T]
-    k_cache: np.ndarray  # uint16 [num_blocks, 16, Hkv, d]
-    v_cache: np.ndarray  # uint16 [num_blocks, 16, Hkv, d]
+    k_cache: np.ndarray  # uint16 [num_blocks, block_size, Hkv, d]
+    v_cache: np.ndarray  # uint16 [num_blocks, block_size, Hkv, d]
     block_tables: np.ndarray  # int32 [B, max_blocks], -1 padded
     context_lens: np.ndarray  # int32 [B], including the step's new tokens
     query_start_loc: np.ndarray  # int32 [B + 1]
@@ -87,6 +87,10 @@ class Batch:
     @property
     def num_blocks(self):
         return self.k_cache.shape[0]
+
+    @property
+    def block_size(self):
+        return self.k_cache.shape[1]
 
 
 def _to_bf16_bits(x32):
@@ -120,15 +124,18 @@ def make_batch(
     shared_seqs=(),
     shared_prefix_blocks=0,
     name="custom",
+    block_size=BLOCK_SIZE,
 ):
     """Build a batch: sequence b holds ``context_lens[b]`` keys after the step, of which the
     last ``spans[b]`` are the step's new tokens (1 = decode, >1 = prefill chunk, 0 = idle).
 
     Physical blocks come from a seeded permutation of the pool.  Sequences listed in
-    ``shared_seqs`` point their first ``min(shared_prefix_blocks, (ctx - 1) // 16)`` logical
-    blocks at one common run of physical blocks (prefix-cache reuse); the block receiving
-    their new token is always private.
+    ``shared_seqs`` point their first ``min(shared_prefix_blocks, (ctx - 1) // block_size)``
+    logical blocks at one common run of physical blocks (prefix-cache reuse); the block
+    receiving their new token is always private.  ``block_size`` is the tokens per pool block
+    (16 unless a block-size variant is being measured).
     """
+    bs = int(block_size)
     rng = np.random.default_rng(seed)
     ctx = np.asarray(context_lens, dtype=np.int64)
     spans = np.asarray(spans, dtype=np.int64)
@@ -138,10 +145,10 @@ def make_batch(
     if np.any(spans > ctx) or np.any(spans < 0):
         raise ValueError("every span must satisfy 0 <= span <= context")
     hq, hkv, d = int(num_q_heads), int(num_kv_heads), int(head_dim)
-    pages = -(-ctx // BLOCK_SIZE)
+    pages = -(-ctx // bs)
     width = int(max_blocks_per_seq) if max_blocks_per_seq else max(1, int(pages.max()) if B else 1)
     if np.any(pages > width):
-        raise ValueError("a context is longer than max_blocks_per_seq * 16")
+        raise ValueError("a context is longer than max_blocks_per_seq * block_size")
 
     perm = rng.permutation(num_blocks).astype(np.int64)
     cursor = 0
@@ -154,7 +161,7 @@ def make_batch(
     for b in range(B):
         n_sh = 0
         if b in shared_set and shared_run is not None:
-            n_sh = min(shared_prefix_blocks, max(0, (int(ctx[b]) - 1) // BLOCK_SIZE))
+            n_sh = min(shared_prefix_blocks, max(0, (int(ctx[b]) - 1) // bs))
             bt[b, :n_sh] = shared_run[:n_sh]
         need = int(pages[b]) - n_sh
         if cursor + need > num_blocks:
@@ -171,7 +178,7 @@ def make_batch(
         n = int(spans[b])
         p = np.arange(int(ctx[b]) - n, int(ctx[b]), dtype=np.int64)
         positions[qsl[b] : qsl[b + 1]] = p
-        slots[qsl[b] : qsl[b + 1]] = bt[b, p // BLOCK_SIZE].astype(np.int64) * BLOCK_SIZE + p % BLOCK_SIZE
+        slots[qsl[b] : qsl[b + 1]] = bt[b, p // bs].astype(np.int64) * bs + p % bs
 
     q = normal_bf16(rng, (T, hq, d))
     k = normal_bf16(rng, (T, hkv, d))
@@ -179,19 +186,19 @@ def make_batch(
 
     # the pool: which (block, row) slots hold context before the step
     used_blocks = np.unique(bt[bt >= 0]).astype(np.int64)
-    row_valid = np.zeros((num_blocks, BLOCK_SIZE), dtype=bool)
+    row_valid = np.zeros((num_blocks, bs), dtype=bool)
     for b in range(B):
         c = int(ctx[b])
         old = c - int(spans[b])  # keys that already exist before the step
-        full, rem = divmod(old, BLOCK_SIZE)
+        full, rem = divmod(old, bs)
         row_valid[bt[b, :full]] = True
         if rem:
             row_valid[bt[b, full], :rem] = True
     caches = []
     for _ in range(2):
-        cache = np.zeros((num_blocks, BLOCK_SIZE, hkv, d), dtype=np.uint16)
+        cache = np.zeros((num_blocks, bs, hkv, d), dtype=np.uint16)
         if used_blocks.size:
-            cache[used_blocks] = normal_bf16(rng, (used_blocks.size, BLOCK_SIZE, hkv, d))
+            cache[used_blocks] = normal_bf16(rng, (used_blocks.size, bs, hkv, d))
         if poison:
             cache[~row_valid] = NAN_BF16
         caches.append(cache)
@@ -223,38 +230,46 @@ CONFIG_NAMES = {
 }
 
 
-def config(index, *, poison=True, seed=None):
-    """The five workloads listed in this module's docstring; seed defaults to index - 1."""
+def config(index, *, poison=True, seed=None, block_size=BLOCK_SIZE):
+    """The five workloads listed in this module's docstring; seed defaults to index - 1.
+
+    ``block_size`` other than 16 builds the same workload over blocks of that many tokens:
+    the pool keeps its capacity in tokens, the table width and the shared prefix their
+    lengths in tokens.  Lengths and sharing do not change; the block permutation does.
+    """
     s = index - 1 if seed is None else seed
-    name = CONFIG_NAMES[index]
+    name = CONFIG_NAMES[index] + ("" if block_size == BLOCK_SIZE else f"-bs{block_size}")
     rng = np.random.default_rng(1000 + s)  # lengths and sharing; values use ``s``
+    bs = int(block_size)
+
+    def blocks(tokens):
+        return -(-tokens // bs)
+
+    kw = dict(poison=poison, name=name, block_size=bs)
     if index == 1:
-        return make_batch([1, 17, 33, 100], [1, 1, 1, 1], 4, 2, 64, 64, s, poison=poison, name=name)
+        return make_batch([1, 17, 33, 100], [1, 1, 1, 1], 4, 2, 64, blocks(64 * 16), s, **kw)
     if index == 2:
         ctx = rng.integers(129, 1152, size=32, endpoint=True)
-        return make_batch(ctx, np.ones(32, np.int64), 14, 2, 64, 4096, s, poison=poison,
-                          scale=1.0 / 8.0, name=name)
+        return make_batch(ctx, np.ones(32, np.int64), 14, 2, 64, blocks(4096 * 16), s, scale=1.0 / 8.0, **kw)
     if index == 3:
         ctx = rng.integers(100, 2048, size=256, endpoint=True)
         shared = rng.permutation(256)[:64]
-        return make_batch(ctx, np.ones(256, np.int64), 16, 8, 128, 40000, s, poison=poison,
-                          max_blocks_per_seq=2048 // BLOCK_SIZE, shared_seqs=shared,
-                          shared_prefix_blocks=32, name=name)
+        return make_batch(ctx, np.ones(256, np.int64), 16, 8, 128, blocks(40000 * 16), s,
+                          max_blocks_per_seq=blocks(2048), shared_seqs=shared,
+                          shared_prefix_blocks=blocks(512), **kw)
     if index == 4:
-        return make_batch(np.full(50, 8192), np.ones(50, np.int64), 28, 4, 128, 26000, s,
-                          poison=poison, name=name)
+        return make_batch(np.full(50, 8192), np.ones(50, np.int64), 28, 4, 128, blocks(26000 * 16), s, **kw)
     if index == 5:
         dec = rng.integers(64, 2048, size=200, endpoint=True)
         prior = np.array([0, 512, 1024, 1536])
         ctx = np.concatenate([dec, prior + 512])
         spans = np.concatenate([np.ones(200, np.int64), np.full(4, 512)])
-        return make_batch(ctx, spans, 16, 8, 128, 20000, s, poison=poison,
-                          max_blocks_per_seq=2048 // BLOCK_SIZE, name=name)
+        return make_batch(ctx, spans, 16, 8, 128, blocks(20000 * 16), s, max_blocks_per_seq=blocks(2048), **kw)
     raise KeyError(index)
 
 
 def random_case(seed, *, max_seqs=3, max_ctx=40, head_dims=(8, 64), groups=(1, 2, 3),
-                kv_heads=(1, 2), allow_prefill=True, poison=True):
+                kv_heads=(1, 2), allow_prefill=True, poison=True, block_size=BLOCK_SIZE):
     """A small random mixed batch for brute-force and micro parity checks."""
     rng = np.random.default_rng(50_000 + seed)
     B = int(rng.integers(1, max_seqs, endpoint=True))
@@ -267,7 +282,8 @@ def random_case(seed, *, max_seqs=3, max_ctx=40, head_dims=(8, 64), groups=(1, 2
         for b in range(B):
             if rng.random() < 0.5:
                 spans[b] = int(rng.integers(1, ctx[b], endpoint=True))
-    pages = int((-(-ctx // BLOCK_SIZE)).sum())
+    pages = int((-(-ctx // block_size)).sum())
     nb = pages + int(rng.integers(0, 8))
     return make_batch(ctx, spans, hq, hkv, d, nb, seed, poison=poison,
-                      rope_theta=float(rng.choice([1.0e4, 1.0e6])), name=f"random-{seed}")
+                      rope_theta=float(rng.choice([1.0e4, 1.0e6])), name=f"random-{seed}",
+                      block_size=block_size)

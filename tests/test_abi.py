@@ -65,7 +65,11 @@ def _append(lib, **kw):
 
 def test_kv_append_host_validation(lib):
     assert _append(lib, d=96) == 5  # head_dim outside the compiled set
-    assert _append(lib, bs=32) == 5  # block_size must be 16
+    for bs in (0, -16, 4, 12, 24, 256):  # block_size: a power of two from 8 to 128
+        assert _append(lib, bs=bs) == 5
+    for bs in (8, 16, 32, 64, 128):
+        assert _append(lib, bs=bs, T=0) == 0  # accepted (a no-op: no tokens)
+    assert _append(lib, nb=1 << 31) == 2  # block ids are int32
     assert _append(lib, hq=6, hkv=4) == 2  # not a multiple
     assert _append(lib, theta=0.0) == 2
     assert _append(lib, T=-1) == 2
@@ -87,7 +91,11 @@ def _attn(lib, **kw):
 
 def test_paged_attention_host_validation(lib):
     assert _attn(lib, d=80) == 5
-    assert _attn(lib, bs=8) == 5
+    for bs in (0, 4, 24, 48, 256):
+        assert _attn(lib, bs=bs) == 5
+    for bs in (8, 16, 32, 64, 128):
+        assert _attn(lib, bs=bs, T=0) == 0
+    assert _attn(lib, nb=1 << 31) == 2
     assert _attn(lib, hq=12, hkv=3) == 5  # 8 decode warps must split evenly over kv heads
     assert _attn(lib, hq=36, hkv=4) == 5  # group of 9 > 8
     assert _attn(lib, hq=6, hkv=4) == 2

@@ -1,0 +1,63 @@
+"""The work planner's counts on the GPU against the oracle's span classification.
+
+The planner writes a small header at the start of the workspace: the number of decode
+spans, the number of decode work units (page groups of 8 / Hkv pages, all kv heads), the
+units per decode CTA, the number of prefill tiles and the number of split partials.  These
+are fixed by the spans and context lengths alone ("09 -- Mini Inference Engine", "Week 3 --
+Continuous batching": a step's batch mixes one-token decode spans with chunked-prefill
+spans; "Week 4 -- Paged KV cache": a sequence of ctx tokens holds ceil(ctx / 16) blocks), so
+they are compared exactly with counts taken from ``oracle.classify_spans``.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.attention import SPAN_DECODE, SPAN_PREFILL
+from paged_kv_gqa_14_gb300 import ops
+from paged_kv_gqa_14_gb300 import workloads as W
+from tests.gpu_util import Dev
+
+pytestmark = pytest.mark.gpu
+
+DECODE_WARPS = 8
+
+
+def _expected(bt, decode_ctas, tile_q):
+    kind, pages, spans = oracle.classify_spans(bt.query_start_loc, bt.context_lens)
+    pps = DECODE_WARPS // bt.num_kv_heads
+    dec = np.flatnonzero(kind == SPAN_DECODE)
+    units = -(-pages[dec] // pps)
+    U = int(units.sum())
+    w = max(1, -(-U // decode_ctas))
+    u0 = np.concatenate([[0], np.cumsum(units)[:-1]]).astype(np.int64)
+    u1 = u0 + units
+    slots = int(((u1 - 1) // w - u0 // w + 1).sum()) if len(dec) else 0
+    tiles = int((-(-spans[kind == SPAN_PREFILL] // tile_q)).sum())
+    return [len(dec), U, w, tiles, slots]
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("prefill", ["mma", "tcgen05"])
+def test_planner_counts_match_oracle_classification(index, prefill):
+    bt = W.config(index, poison=False)
+    d = Dev(bt)
+    T, hq, hd = bt.q.shape
+    mb = bt.block_tables.shape[1]
+    ctas = 100
+    ops.set_decode_ctas(ctas)
+    ops.set_prefill_kernel(prefill)
+    try:
+        ws = ops.alloc_workspace(T, bt.num_seqs, hq, bt.num_kv_heads, hd, mb, device=d.q.device)
+        ws.fill_(0xFF)
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                            workspace=ws)
+        torch.cuda.synchronize()
+        assert ops.get_device_error() == 0
+        header = ws[:20].cpu().numpy().view(np.int32)[:5].tolist()
+    finally:
+        ops.set_decode_ctas(0)
+        ops.set_prefill_kernel("auto")
+    tile_q = 128 if prefill == "tcgen05" else 64
+    assert header == _expected(bt, ctas, tile_q)
