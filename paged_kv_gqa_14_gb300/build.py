@@ -19,7 +19,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 
-SOURCES = ["abi.cu", "kv_append.cu", "attention.cu", "noalloc.cu"]
+# (source, object name, extra flags): decode_tc.cu is built once per pool block size
+SOURCES = [("abi.cu", "abi.o", []), ("kv_append.cu", "kv_append.o", []), ("attention.cu", "attention.o", []),
+           ("noalloc.cu", "noalloc.o", [])] + [
+    ("decode_tc.cu", f"decode_tc_bs{bs}.o", [f"-DPKV_DECODE_TC_BS={bs}"]) for bs in (8, 16, 32, 64, 128)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No --use_fast_math: sincosf in the RoPE kernel stays the accurate library routine; the
 # kernels call fast approximations (ex2.approx) explicitly where they want them.
@@ -59,14 +62,14 @@ def build(force=False, verbose=False, ptxas_info=False):
     cc = nvcc()
     procs = []
     objs = []
-    for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
+    for src, oname, extra in SOURCES:
+        obj = os.path.join(BUILD, oname)
+        cmd = [cc, *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]
         if verbose:
             print(" ".join(cmd), flush=True)
-        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
+        procs.append((oname, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
         objs.append(obj)
     failed = []
     for src, p in procs:

@@ -18,6 +18,44 @@
 #include "prefill_tc.cuh"
 
 namespace pkv {
+
+// cuTensorMapEncodeTiled, fetched from the driver once (no link-time dependency on libcuda)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// The pool [num_blocks][block_size][Hkv][d] as a 4-D tensor {d, Hkv, block_size, num_blocks};
+// a box is min(block_size, 16) token rows x 64 dims of one kv head in one block, 128-byte
+// swizzled.
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t bs = cuuint64_t(1) << bs_log2;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv), bs,
+                              static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hkv) * D * 2,
+                                 bs * hkv * D * 2};
+  const cuuint32_t box[4] = {64, 1, bs < 16 ? static_cast<cuuint32_t>(bs) : 16u, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 constexpr int kPlanThreads = 1024;
@@ -215,105 +253,17 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   return e;
 }
 
-// cuTensorMapEncodeTiled, fetched from the driver once (no link-time dependency on libcuda)
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// The pool [num_blocks][block_size][Hkv][d] as a 4-D tensor {d, Hkv, block_size, num_blocks};
-// a box is min(block_size, 16) token rows x 64 dims of one kv head in one block, 128-byte
-// swizzled.
-bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t bs = cuuint64_t(1) << bs_log2;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv), bs,
-                              static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hkv) * D * 2,
-                                 bs * hkv * D * 2};
-  const cuuint32_t box[4] = {64, 1, bs < 16 ? static_cast<cuuint32_t>(bs) : 16u, 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int D, int G, int BS>
-cudaError_t launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
-  using C = DecodeTcCfg<D, G>;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  DecodeTcParams P;
-  if (!make_pool_map(&P.tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, D) ||
-      !make_pool_map(&P.tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, D))
-    return cudaErrorInvalidValue;
-  DecodeParams& p = P.p;
-  p.q = static_cast<const bf16*>(a.q);
-  p.q_st = a.q_st;
-  p.q_sh = a.q_sh;
-  p.k_cache = static_cast<const bf16*>(a.k_cache);
-  p.v_cache = static_cast<const bf16*>(a.v_cache);
-  p.num_blocks = a.num_blocks;
-  p.bs_log2 = a.bs_log2;
-  p.block_tables = a.block_tables;
-  p.bt_stride = a.bt_stride;
-  p.context_lens = a.context_lens;
-  p.qsl = a.qsl;
-  p.out = static_cast<bf16*>(a.out);
-  p.o_st = a.o_st;
-  p.o_sh = a.o_sh;
-  p.hkv = a.hkv;
-  p.hq = a.hq;
-  p.qscale = a.scale * 1.4426950408889634f;
-  p.plan = a.plan;
-  p.err = a.err;
-  record_kernel_event(PKV_KERNEL_DECODE, false, stream);
-  const cudaError_t e = launch_pdl(decode_tc_kernel<D, G, BS>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
-                                   C::kSmemBytes, stream, P);
-  record_kernel_event(PKV_KERNEL_DECODE, true, stream);
-  return e;
-}
-
-template <int D, int G>
-cudaError_t launch_decode_pick(const AttnArgs& a, cudaStream_t stream) {
-  const int kind = a.decode_kernel != 0 ? a.decode_kernel : (G >= kTensorDecodeMinGroup ? 2 : 1);
-  if (kind != 2) return launch_decode<D, G>(a, stream);
-  // 16-token blocks get the instance with the block size folded in
-  return a.bs_log2 == 4 ? launch_decode_tc<D, G, 16>(a, stream) : launch_decode_tc<D, G, 0>(a, stream);
-}
-
 template <int D>
 cudaError_t launch_decode_g(const AttnArgs& a, cudaStream_t stream) {
   switch (a.hq / a.hkv) {
-    case 1: return launch_decode_pick<D, 1>(a, stream);
-    case 2: return launch_decode_pick<D, 2>(a, stream);
-    case 3: return launch_decode_pick<D, 3>(a, stream);
-    case 4: return launch_decode_pick<D, 4>(a, stream);
-    case 5: return launch_decode_pick<D, 5>(a, stream);
-    case 6: return launch_decode_pick<D, 6>(a, stream);
-    case 7: return launch_decode_pick<D, 7>(a, stream);
-    case 8: return launch_decode_pick<D, 8>(a, stream);
+    case 1: return launch_decode<D, 1>(a, stream);
+    case 2: return launch_decode<D, 2>(a, stream);
+    case 3: return launch_decode<D, 3>(a, stream);
+    case 4: return launch_decode<D, 4>(a, stream);
+    case 5: return launch_decode<D, 5>(a, stream);
+    case 6: return launch_decode<D, 6>(a, stream);
+    case 7: return launch_decode<D, 7>(a, stream);
+    case 8: return launch_decode<D, 8>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -385,6 +335,17 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   else
     e = (a.head_dim == 128) ? launch_prefill<128>(a, stream) : launch_prefill<64>(a, stream);
   if (e != cudaSuccess) return e;
+  const int kind = a.decode_kernel != 0 ? a.decode_kernel : (a.hq / a.hkv >= kTensorDecodeMinGroup ? 2 : 1);
+  if (kind == 2) {
+    switch (a.bs_log2) {  // one compiled instance per block size (decode_tc.cu)
+      case 3: return launch_decode_tc_bs8(a, stream);
+      case 4: return launch_decode_tc_bs16(a, stream);
+      case 5: return launch_decode_tc_bs32(a, stream);
+      case 6: return launch_decode_tc_bs64(a, stream);
+      case 7: return launch_decode_tc_bs128(a, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   return (a.head_dim == 128) ? launch_decode_g<128>(a, stream) : launch_decode_g<64>(a, stream);
 }
 

@@ -21,11 +21,11 @@
 // 8-token blocks it is two boxes of 8 rows from two blocks, landing 1024 bytes apart, which
 // with the 128-byte swizzle is the same shared-memory image as one 16-row box.
 //
-// The producer is instantiated twice: for 16-token blocks (the default pool) with the block
-// size folded in at compile time, and for every other block size with it read at run time.
-// The kernel is sensitive to the producer warp's instruction stream (it shares a scheduler
-// with two consumer warps and sits on the ring's refill path): on GB300 the run-time form
-// costs about 8% of decode time at 16-token blocks, the compile-time form nothing.
+// The kernel is instantiated per block size, with it folded in at compile time.  The decode
+// is sensitive to the producer warp's instruction stream (the warp shares a scheduler with
+// two consumer warps and sits on the ring's refill path): on GB300 a form reading the block
+// size at run time cost about 8% of decode time at 16-token blocks.  The instances live in
+// decode_tc.cu, built once per block size.
 #pragma once
 
 #include <cuda.h>
@@ -96,7 +96,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // byte offset of 16-byte chunk `c` (0..7) of token row `t` inside a 128B-swizzled box
 __device__ __forceinline__ uint32_t box_off(int t, int c) { return t * 128 + ((c ^ (t & 7)) << 4); }
 
-// BS: 16 for pools of 16-token blocks, 0 for any other block size (read from the params).
+// BS: tokens per pool block, a power of two from 8 to 128.
 template <int D, int G, int BS>
 __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams P) {
@@ -174,9 +174,10 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     int npages = ceil_div(ctx, 16);
     // page gp: block gp >> s4 and its rows from (16 gp) & bmask when blocks hold 16 << s4
     // tokens; blocks 2 gp and 2 gp + 1 (the second only if it holds context) when they hold 8
-    const int sh = BS == 16 ? 4 : p.bs_log2;
-    const int bmask = (1 << sh) - 1;
-    const bool two_blocks = BS == 16 ? false : sh == 3;
+    constexpr int sh = BS == 8 ? 3 : BS == 16 ? 4 : BS == 32 ? 5 : BS == 64 ? 6 : 7;
+    static_assert((1 << sh) == BS, "block size must be a power of two from 8 to 128");
+    constexpr int bmask = BS - 1;
+    constexpr bool two_blocks = BS == 8;
     int it = 0;
     for (int u = ubeg; u < uend; ++u, ++it) {
       while (u >= unext) {
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
       const int gp = pg0 + bp;
       if (issue) {
         const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
-        blk = row[two_blocks ? 2 * gp : gp >> (sh - 4)];
+        blk = row[two_blocks ? 2 * gp : gp >> (sh >= 4 ? sh - 4 : 0)];
         if (blk < 0 || blk >= p.num_blocks) {
           raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
           blk = 0;
@@ -410,5 +411,9 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     ++i;
   }
 }
+
+// The pool [num_blocks][block_size][Hkv][d] as a 4-D tensor map for the tensor-core
+// kernels (defined in attention.cu).
+bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D);
 
 }  // namespace pkv

@@ -115,6 +115,12 @@ struct AttnArgs {
   unsigned int* err;
 };
 cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream);
+// The tensor-core decode for each pool block size (decode_tc.cu, built once per size).
+cudaError_t launch_decode_tc_bs8(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_tc_bs16(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_tc_bs32(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_tc_bs64(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_tc_bs128(const AttnArgs& a, cudaStream_t stream);
 
 int device_sm_count();
 
