@@ -42,13 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # ------------------------------------------------------------------------ workload facts
-def kv_unique_bytes(bt):
-    """K+V bytes of every distinct (physical slot, kv head) the step's attention reads."""
+def kv_unique_bytes(bt, spans=None):
+    """K+V bytes of every distinct (physical slot, kv head) the step's attention reads; with
+    ``spans`` given, only over the sequences whose span length is in it."""
     bs = bt.block_size
     rows = set()
     for b in range(bt.num_seqs):
         n = int(bt.query_start_loc[b + 1] - bt.query_start_loc[b])
-        if n == 0:
+        if n == 0 or (spans is not None and n not in spans):
             continue
         ctx = int(bt.context_lens[b])
         for j in range(-(-ctx // bs)):
@@ -63,11 +64,16 @@ def kv_logical_bytes(bt):
     return int(bt.context_lens[spans > 0].astype(np.int64).sum()) * bt.num_kv_heads * bt.head_dim * 2 * 2
 
 
-def decode_algorithmic_bytes(bt, kv_unique):
-    """Algorithmic bytes of one decode-kernel launch: unique KV + q read + out write + tables."""
-    qo = 2 * bt.num_tokens * bt.num_q_heads * bt.head_dim * 2
-    tables = int((-(-bt.context_lens.astype(np.int64) // bt.block_size)).sum()) * 4 + bt.num_seqs * 8
-    return kv_unique + qo + tables
+def decode_algorithmic_bytes(bt):
+    """Algorithmic bytes of one decode-kernel launch: the unique KV of the decode sequences
+    (span 1), their q rows read and out rows written, and their block-table entries and
+    per-sequence metadata.  Prefill spans are the prefill kernel's."""
+    spans = np.diff(bt.query_start_loc)
+    dec = spans == 1
+    kv = kv_unique_bytes(bt, spans=(1,))
+    qo = 2 * int(dec.sum()) * bt.num_q_heads * bt.head_dim * 2
+    tables = int((-(-bt.context_lens[dec].astype(np.int64) // bt.block_size)).sum()) * 4 + int(dec.sum()) * 8
+    return kv + qo + tables
 
 
 def sub_batch(bt, seqs):
@@ -181,27 +187,36 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_traffic(bt_name, algorithmic_bytes):
-    """Per-launch DRAM traffic of the decode kernel from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+def decode_traffic(bt_name):
+    """Per-launch DRAM traffic of the decode kernel from the committed ncu summary
+    (profiles/decode_tc_traffic_decode-workloads.md), if it was taken on the current kernel
+    sources and covers this workload; else None."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    path = os.path.join(ROOT, "profiles", "decode_tc_traffic_decode-workloads.md")
     try:
         with open(path) as f:
-            rec = json.load(f)
-    except (OSError, ValueError):
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    rec = {}
+    for line in lines:
+        if line.startswith("source_sha256:"):
+            rec["sha"] = line.split(":", 1)[1].strip()
+        elif line.startswith("sources:"):
+            rec["sources"] = [x.strip() for x in line.split(":", 1)[1].split(",")]
+        elif line.startswith("| ") and line.split("|")[1].strip() == bt_name:
+            rec["bytes"] = float(line.split("|")[7])
+    if "bytes" not in rec or "sha" not in rec:
         return None
     h = hashlib.sha256()
-    for name in rec.get("sources", []):
-        with open(os.path.join(ROOT, name), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest() != rec.get("source_sha256"):
+    try:
+        for name in rec.get("sources", []):
+            with open(os.path.join(ROOT, name), "rb") as f:
+                h.update(f.read())
+    except OSError:
         return None
-    entry = rec.get("workloads", {}).get(bt_name)
-    if not entry:
-        return None
-    return float(entry["dram_bytes_per_launch"])
+    return rec["bytes"] if h.hexdigest() == rec["sha"] else None
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -229,7 +244,7 @@ def run_gpu(args, rank, world, local_rank):
         bt = sub_batch(bt, range(min(args.seqs, bt.num_seqs)))
     kv_u = kv_unique_bytes(bt)
     kv_l = kv_logical_bytes(bt)
-    algo = decode_algorithmic_bytes(bt, kv_u)
+    algo = decode_algorithmic_bytes(bt)
     n_decode = int((np.diff(bt.query_start_loc) == 1).sum())
 
     def up(a):
@@ -302,7 +317,7 @@ def run_gpu(args, rank, world, local_rank):
     dec_avg = sum(dec_ms) / K
     peak, peak_kind = hbm_peak()
     achieved = algo / (dec_avg * 1e-3) / 1e9
-    traffic = decode_traffic(bt.name, algo)
+    traffic = decode_traffic(bt.name)
 
     # the same step captured once in a CUDA graph and replayed (host launch cost removed)
     graph = torch.cuda.CUDAGraph()

@@ -197,17 +197,16 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
       const int gp = pg0 + bp;
       if (issue) {
         const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
+        // both reads are issued before either is checked, so their latencies overlap
         blk = row[two_blocks ? 2 * gp : gp >> (sh >= 4 ? sh - 4 : 0)];
+        if (two_blocks && gp * 16 + 8 < ctx) blk2 = row[2 * gp + 1];
         if (blk < 0 || blk >= p.num_blocks) {
           raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
           blk = 0;
         }
-        if (two_blocks && gp * 16 + 8 < ctx) {
-          blk2 = row[2 * gp + 1];
-          if (blk2 < 0 || blk2 >= p.num_blocks) {
-            raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
-            blk2 = 0;
-          }
+        if (two_blocks && gp * 16 + 8 < ctx && (blk2 < 0 || blk2 >= p.num_blocks)) {
+          raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+          blk2 = 0;
         }
       }
       // a last half page past the context is not loaded (8-token blocks)
