@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     if (i < n_dec) {
       plan.dec_slot[i] = ex.a + carry2;
       plan.dec_chunks[i] = v.a;
+      // the decode CTAs whose first unit c W falls in this sequence's units [u0, u1)
+      const int u0 = plan.dec_unit[i], u1 = plan.dec_unit[i + 1];
+      for (int c = ceil_div(u0, W); c * W < u1; ++c) plan.cta_first[c] = i;
     }
     __syncthreads();
     if (threadIdx.x == 0) carry2 += tot.a;
@@ -375,6 +378,8 @@ PlanSizes plan_sizes(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads, 
   off = align256(off + num_seqs * sizeof(int));
   s.off_dec_count = off;
   off = align256(off + num_seqs * sizeof(int));
+  s.off_cta_first = off;
+  off = align256(off + decode_ctas * sizeof(int));
   s.off_pf_seq = off;
   off = align256(off + s.max_tiles * sizeof(int));
   s.off_pf_tile = off;
@@ -396,6 +401,7 @@ Plan plan_view(void* workspace, const PlanSizes& s) {
   p.dec_slot = reinterpret_cast<int*>(w + s.off_dec_slot);
   p.dec_chunks = reinterpret_cast<int*>(w + s.off_dec_chunks);
   p.dec_count = reinterpret_cast<int*>(w + s.off_dec_count);
+  p.cta_first = reinterpret_cast<int*>(w + s.off_cta_first);
   p.pf_seq = reinterpret_cast<int*>(w + s.off_pf_seq);
   p.pf_tile = reinterpret_cast<int*>(w + s.off_pf_tile);
   p.part_ml = reinterpret_cast<float*>(w + s.off_part_ml);

@@ -170,7 +170,6 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
   uint64_t* empty = full + STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
-  int* seg0 = const_cast<int*>(reinterpret_cast<volatile int*>(abort_flag + 1));
   volatile int* last_flag = abort_flag + 2;
   float* pbuf = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes + C::kBarBytes);
   float* xbuf = pbuf + kDecodeWarps * 16 * G;
@@ -188,25 +187,16 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   pdl_wait();  // the plan is written by the planner kernel
   pdl_trigger();
   const int* hdr = p.plan.header;
-  const int n_dec = hdr[0];
   const int U = hdr[1];
   const int W = hdr[2];
+  // the decode sequence holding this CTA's first unit, from the planner (read alongside the
+  // header; meaningless, and unused, for a CTA without units)
+  const int i_first = p.plan.cta_first[blockIdx.x];
   const int ubeg = blockIdx.x * W;
   const int uend = min(U, ubeg + W);
   if (ubeg >= uend) return;  // CTA-uniform
-
   const int* dec_unit = p.plan.dec_unit;
-  if (threadIdx.x == 0) {
-    // the decode sequence holding unit ubeg: largest i with dec_unit[i] <= ubeg
-    int lo = 0, hi = n_dec - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (dec_unit[mid] <= ubeg) lo = mid; else hi = mid - 1;
-    }
-    *seg0 = lo;
-  }
-  __syncthreads();
-  const int i_first = *seg0;
+  __syncthreads();  // barrier initialisation visible to every warp
 
   const int hkv = p.hkv;
   const int pps = kDecodeWarps / hkv;

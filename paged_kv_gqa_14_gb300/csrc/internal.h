@@ -47,6 +47,8 @@ struct Plan {
   int* dec_slot;    // [B]      first partial slot of each decode sequence
   int* dec_chunks;  // [B]      number of decode CTAs that touch the sequence
   int* dec_count;   // [B]      split states written so far (zeroed by the planner)
+  int* cta_first;   // [C]      decode CTA c: index in the decode list of the sequence holding
+                    //          its first unit c W (written only for CTAs that have units)
   int* pf_seq;      // [max_tiles]  prefill work item: sequence id
   int* pf_tile;     // [max_tiles]  prefill work item: q-tile index within the span
   float* part_ml;   // [S_max][Hq][2]   split state: running max (log2 domain), sum of weights
@@ -56,7 +58,7 @@ struct Plan {
 struct PlanSizes {
   int64_t num_seqs, num_tokens, num_q_heads, head_dim, decode_ctas;
   int64_t max_tiles, max_slots;
-  size_t off_header, off_dec_seq, off_dec_unit, off_dec_slot, off_dec_chunks, off_dec_count;
+  size_t off_header, off_dec_seq, off_dec_unit, off_dec_slot, off_dec_chunks, off_dec_count, off_cta_first;
   size_t off_pf_seq, off_pf_tile, off_part_ml, off_part_acc, total;
 };
 
