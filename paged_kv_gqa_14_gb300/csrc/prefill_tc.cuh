@@ -323,13 +323,26 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
         tc5::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[s]);
-        float mx = NEG_INF;
+        // row max of the raw scores (qscale > 0 keeps the order, and fl(max * qscale) is the max
+        // of the scaled scores), over eight independent partial maxima; the mask is a select
+        // and only the diagonal tiles need it
         const int key0 = jt * C::BK;
+        float mx8[8];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          sc[c] = (live && key0 + c <= pos) ? sc[c] * p.qscale : NEG_INF;
-          mx = fmaxf(mx, sc[c]);
+        for (int x = 0; x < 8; ++x) mx8[x] = NEG_INF;
+        if (live && key0 + C::BK - 1 <= pos) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            sc[c] = (live && key0 + c <= pos) ? sc[c] : NEG_INF;
+            mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
+          }
         }
+        const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mx = mraw * p.qscale;  // -inf stays -inf
         float corr = 1.f;
         bool resc = false;
         if (m_run == NEG_INF) {
@@ -340,12 +353,16 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
           resc = true;
         }
         const float base = m_run == NEG_INF ? 0.f : m_run;
-        float lsum = 0.f;
+        // p = 2^(s * qscale - base): one FFMA and one ex2 per score; eight partial sums
+        float ls8[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) ls8[x] = 0.f;
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
-          sc[c] = fast_exp2(sc[c] - base);
-          lsum += sc[c];
+          sc[c] = fast_exp2(fmaf(sc[c], p.qscale, -base));
+          ls8[c & 7] += sc[c];
         }
+        const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
         l_run = l_run * corr + lsum;
         if (jt > 0) {
           ok = warp_wait(pv_done, (f - 1) & 1, p.err, abort_flag);  // P buffer free, O stable
