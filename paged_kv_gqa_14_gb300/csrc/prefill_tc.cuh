@@ -6,16 +6,19 @@
 // position ctx - n + r and sees keys 0 .. ctx - n + r.
 //
 // Per item, one CTA of eight warps with fixed roles:
-//   warp 0     TMA producer: the Q tile once (3-D tensor map over q), then K and V tiles of
+//   warp 0     TMA producer: the Q tile once (3-D tensor map over q), then the K tiles of
 //              128 keys = 8 pages gathered through the block table (4-D pool map, one box
 //              per page x kv head x 64 dims), into a 2-stage ring.
 //   warp 1     allocates TMEM (S double buffer: 2 x 128 columns; O: d columns) and, from one
 //              thread, issues   S = Q . K^T   (M 128, N 128, K d)   and
 //                               O += P . V    (M 128, N d,   K 128)  as tcgen05.mma kind::f16,
-//              bf16 operands from shared memory, fp32 accumulators in TMEM, completion
-//              signalled with tcgen05.commit on mbarriers.
-//   warps 2-3  transpose each V tile into V^T (ldmatrix.trans / stmatrix) so that both
-//              operands of every MMA are K-major; keys past the visible range become 0.
+//              bf16 operands from shared memory (Q, K, P K-major; V read as it lands, an
+//              MN-major operand), fp32 accumulators in TMEM, completion signalled with
+//              tcgen05.commit on mbarriers.
+//   warps 2-3  warp 2 loads the V tiles the same way into their own 2-stage ring (so a K load
+//              never waits for a V stage); both release each V tile to the MMA, in an item's
+//              last tile after zeroing the rows of keys past the visible range (unloaded or
+//              past the context: 0 * NaN would poison O).
 //   warps 4-7  softmax: thread = query row.  Reads its S row from TMEM, masks by select,
 //              keeps a running max m and sum l in the log2 domain and writes P (bf16) to
 //              shared memory.  O in TMEM is rescaled only when the row max grows by more
@@ -48,13 +51,11 @@ struct PrefillTcCfg {
   static constexpr int kBlk = 128 * 128;  // one [128 rows][64 elements] swizzled block: 16 KB
   static constexpr int kQBytes = BQ * D * 2;
   static constexpr int kKVBytes = BK * D * 2;
-  static constexpr int kVtBytes = D * BK * 2;
   static constexpr int kPBytes = BQ * BK * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + kQBytes;       // 2 stages
   static constexpr int OFF_V = OFF_K + 2 * kKVBytes;  // 2 stages
-  static constexpr int OFF_VT = OFF_V + 2 * kKVBytes;
-  static constexpr int OFF_P = OFF_VT + kVtBytes;
+  static constexpr int OFF_P = OFF_V + 2 * kKVBytes;
   static constexpr int OFF_BAR = OFF_P + kPBytes;
   static constexpr int kSmemBytes = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -69,12 +70,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* m
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
-               "r"(r[2]), "r"(r[3])
-               : "memory");
 }
 
 // All 32 lanes wait; the outcome is made warp-uniform (any lane timing out aborts the warp).
@@ -98,7 +93,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   uint64_t* k_full = bars + 1;   // [2]
   uint64_t* v_full = bars + 3;   // [2]
   uint64_t* k_empty = bars + 5;  // [2] MMA finished reading the K stage
-  uint64_t* v_empty = bars + 7;  // [2] transposers finished reading the V stage
+  uint64_t* v_empty = bars + 7;  // [2] the P.V MMA finished reading the V stage
   uint64_t* s_full = bars + 9;   // [2] S buffer written
   uint64_t* s_free = bars + 11;  // [2] softmax finished reading the S buffer
   uint64_t* vt_full = bars + 13;
@@ -116,7 +111,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 2);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], 4);
     }
@@ -172,73 +167,73 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
     const int nkt = ceil_div(kv_end, C::BK);
     const int npages = ceil_div(kv_end, 16);
 
+    // One K or V tile of 128 keys = 8 pages, issued by one warp (lane = page x 64-dim half):
+    // 16-token pages are rows 16j..16j+15 of one block, or (8-token blocks) two boxes of 8
+    // rows from two blocks, 1024 bytes apart in shared memory; a last half page past kv_end
+    // is not loaded (its block may not exist, and those keys are never used).
+    auto load_tile = [&](bool is_v, int jt, int s) {
+      constexpr int per = 8 * HALVES;
+      const int bmask = (1 << p.bs_log2) - 1;
+      const int box_rows = p.bs_log2 >= 4 ? 16 : 8;  // the tensor map's box height
+      const int pg = lane / HALVES;
+      const int half = lane - pg * HALVES;
+      const int npg = min(8, npages - jt * 8);
+      const bool tail_half = box_rows == 8 && jt * C::BK + (npg - 1) * 16 + 8 >= kv_end;
+      const uint32_t tile_bytes = static_cast<uint32_t>((npg * 2 - (tail_half ? 1 : 0)) * HALVES * 1024);
+      uint64_t* bar = is_v ? &v_full[s] : &k_full[s];
+      if (lane == 0) mbar_arrive_expect_tx(bar, tile_bytes);
+      __syncwarp();
+      if (lane < per && pg < npg) {
+        unsigned char* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s * C::kKVBytes + half * C::kBlk + pg * 2048;
+        const int tok = jt * C::BK + pg * 16;
+        for (int r = 0; r < 16 && tok + r < kv_end; r += box_rows) {
+          const int tr = tok + r;
+          int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (tr >> p.bs_log2)];
+          if (blk < 0 || blk >= p.num_blocks) {
+            raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+            blk = 0;
+          }
+          tma_load_4d(dst + r * 128, is_v ? &P.tmap_v : &P.tmap_k, half * 64, h, tr & bmask, blk, bar, pol);
+        }
+      }
+    };
+
     if (warp == 0) {
-      // ------------------------------------------------------------------ TMA producer
+      // ---------------------------------------------------------- TMA producer: Q and K
       bool ok = !*abort_flag;
       if (ok) {
         if (lane == 0) mbar_arrive_expect_tx(q_full, C::kQBytes);
         __syncwarp();
         if (lane < HALVES) tma_load_3d(smem + C::OFF_Q + lane * C::kBlk, &P.tmap_q, lane * 64, hq, s0 + q0, q_full);
       }
-      const int per = 8 * HALVES;  // 16-row boxes per K (or V) tile
-      const int bmask = (1 << p.bs_log2) - 1;
-      const int box_rows = p.bs_log2 >= 4 ? 16 : 8;  // the tensor map's box height
-      const int kv = lane / per;
-      const int rem = lane - kv * per;
-      const int pg = rem / HALVES;
-      const int half = rem - pg * HALVES;
       for (int jt = 0; jt < nkt && ok; ++jt) {
         const int f = t_glob + jt;
         const int s = f & 1;
         if (f >= 2) {
-          ok = warp_wait(&k_empty[s], ((f >> 1) - 1) & 1, p.err, abort_flag) &&
-               warp_wait(&v_empty[s], ((f >> 1) - 1) & 1, p.err, abort_flag);
+          ok = warp_wait(&k_empty[s], ((f >> 1) - 1) & 1, p.err, abort_flag);
           if (!ok) break;
         }
-        const int npg = min(8, npages - jt * 8);
-        // 16-token pages: rows 16j..16j+15 of one block, or (8-token blocks) two boxes of 8
-        // rows from two blocks, 1024 bytes apart in shared memory; a last half past kv_end
-        // is not loaded (its block may not exist, and those keys are masked)
-        const bool tail_half = box_rows == 8 && jt * C::BK + (npg - 1) * 16 + 8 >= kv_end;
-        const uint32_t tile_bytes = static_cast<uint32_t>((npg * 2 - (tail_half ? 1 : 0)) * HALVES * 1024);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&k_full[s], tile_bytes);
-          mbar_arrive_expect_tx(&v_full[s], tile_bytes);
-        }
-        __syncwarp();
-        if (lane < 2 * per && pg < npg) {
-          unsigned char* dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::kKVBytes + half * C::kBlk + pg * 2048;
-          const int tok = jt * C::BK + pg * 16;
-          for (int r = 0; r < 16 && tok + r < kv_end; r += box_rows) {
-            const int tr = tok + r;
-            int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (tr >> p.bs_log2)];
-            if (blk < 0 || blk >= p.num_blocks) {
-              raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
-              blk = 0;
-            }
-            tma_load_4d(dst + r * 128, kv ? &P.tmap_v : &P.tmap_k, half * 64, h, tr & bmask, blk,
-                        kv ? &v_full[s] : &k_full[s], pol);
-          }
-        }
+        load_tile(false, jt, s);
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------------- MMA issuer
       if (lane == 0) {
         constexpr uint32_t kIdescQK = tc5::idesc_bf16_f32(128, 128);
-        constexpr uint32_t kIdescPV = tc5::idesc_bf16_f32(128, D);
+        constexpr uint32_t kIdescPV = tc5::idesc_bf16_f32(128, D, true);
         bool ok = wait_or_abort(q_full, item_no & 1, p.err, abort_flag);
         auto issue_pv = [&](int fp, bool first) -> bool {
           if (!wait_or_abort(vt_full, fp & 1, p.err, abort_flag)) return false;
           if (!wait_or_abort(p_full, fp & 1, p.err, abort_flag)) return false;
           tc5::fence_after();
+          const uint32_t vst = sb + C::OFF_V + (fp & 1) * C::kKVBytes;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlk + (kk & 3) * 32;
-            const uint32_t offv = (kk >> 2) * (D * 128) + (kk & 3) * 32;
             tc5::mma_ss(tmem + C::COL_O, tc5::smem_desc_k128(sb + C::OFF_P + off),
-                        tc5::smem_desc_k128(sb + C::OFF_VT + offv), kIdescPV, (first && kk == 0) ? 0u : 1u);
+                        tc5::smem_desc_mn128(vst + kk * 2048, C::kBlk), kIdescPV, (first && kk == 0) ? 0u : 1u);
           }
           tc5::commit(pv_done);
+          tc5::commit(&v_empty[fp & 1]);
           return true;
         };
         for (int jt = 0; jt < nkt && ok; ++jt) {
@@ -262,39 +257,36 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
       }
       __syncwarp();
     } else if (warp < 4) {
-      // ------------------------------------------------------- V -> V^T transposers
+      // ------------------------------------------------- V loads (warp 2) and release
+      // Tile f is released after P.V of tile f - 1 was issued and completed (pv_done), which
+      // also keeps this barrier at most one phase ahead of the MMA thread's waits.
       const int tw = warp - 2;
       bool ok = !*abort_flag;
       for (int jt = 0; jt < nkt && ok; ++jt) {
         const int f = t_glob + jt;
         const int s = f & 1;
+        if (tw == 0) {  // warp 2 also loads the V tiles, each as soon as P.V freed its stage
+          if (f >= 2) ok = warp_wait(&v_empty[s], ((f >> 1) - 1) & 1, p.err, abort_flag);
+          if (!ok) break;
+          load_tile(true, jt, s);
+        }
         ok = warp_wait(&v_full[s], (f >> 1) & 1, p.err, abort_flag);
-        if (ok && f >= 1) ok = warp_wait(pv_done, (f - 1) & 1, p.err, abort_flag);  // V^T buffer free
+        if (ok && f >= 1) ok = warp_wait(pv_done, (f - 1) & 1, p.err, abort_flag);
         if (!ok) break;
-        const uint32_t vbase = sb + C::OFF_V + s * C::kKVBytes;
-        const uint32_t tbase = sb + C::OFF_VT;
-        constexpr int DG = D / 32;  // groups of four 8-dim chunks
-        for (int o = tw; o < 16 * DG; o += 2) {
-          const int kb = o / DG;  // 8-key block
-          const int dg = o - kb * DG;
-          const int i = lane >> 3;
-          const int dc = 4 * dg + i;  // 8-dim chunk of this lane's source row
-          const int kr = 8 * kb + (lane & 7);
-          uint32_t r[4];
-          ldsm_x4_t_tc(r, vbase + (dc >> 3) * C::kBlk + box_off(kr, dc & 7));
-          const int key = jt * C::BK + 8 * kb + 2 * (lane & 3);
-          const uint32_t keep = (key < kv_end ? 0x0000ffffu : 0u) | (key + 1 < kv_end ? 0xffff0000u : 0u);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) r[x] &= keep;
-          const int dr = 8 * dc + (lane & 7);  // V^T row = head dim
-          stsm_x4(tbase + (kb >> 3) * (D * 128) + box_off(dr, kb & 7), r);
+        const int vis = kv_end - jt * C::BK;  // keys of this tile that some row sees
+        if (vis < C::BK) {
+          unsigned char* vbase = smem + C::OFF_V + s * C::kKVBytes;
+          const int n16 = (C::BK - vis) * 8 * HALVES;  // 16-byte chunks to clear
+          for (int idx = tw * 32 + lane; idx < n16; idx += 64) {
+            const int hh = idx / ((C::BK - vis) * 8);
+            const int rem = idx - hh * (C::BK - vis) * 8;
+            *reinterpret_cast<uint4*>(vbase + hh * C::kBlk + (vis + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&v_empty[s]);
-          mbar_arrive(vt_full);
-        }
+        if (lane == 0) mbar_arrive(vt_full);
       }
     } else {
       // -------------------------------------------------------------------- softmax

@@ -28,12 +28,27 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor of a dense kind::f16 MMA: bf16 A and B (both K-major), fp32 D,
-// shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Shared-memory matrix descriptor for an MN-major, 128B-swizzled operand: rows of 64
+// MN-elements (128 bytes) indexed by K, eight K-rows per 1024-byte atom (atoms along K
+// 1024 bytes apart), and the next 64 MN-elements `mn_block_bytes` further on.  `addr` is the
+// shared address of the K-slice's first row (a K step of 16 rows advances it by 2048 bytes).
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t addr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);           // start address
+  d |= static_cast<uint64_t>(mn_block_bytes >> 4) << 16;          // leading byte offset: next 64 MN
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                    // stride byte offset: next 8 K-rows
+  d |= static_cast<uint64_t>(1) << 46;                            // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                            // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of a dense kind::f16 MMA: bf16 A (K-major) and B (K-major, or
+// MN-major when b_mn_major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false) {
   return (1u << 4)                                    // D format: f32
          | (1u << 7)                                  // A format: bf16
          | (1u << 10)                                 // B format: bf16
+         | (b_mn_major ? (1u << 16) : 0u)             // B major-ness: MN-major
          | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
 }
