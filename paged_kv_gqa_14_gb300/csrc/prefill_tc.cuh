@@ -8,17 +8,18 @@
 // Per item, one CTA of eight warps with fixed roles:
 //   warp 0     TMA producer: the Q tile once (3-D tensor map over q), then the K tiles of
 //              128 keys = 8 pages gathered through the block table (4-D pool map, one box
-//              per page x kv head x 64 dims), into a 2-stage ring.
+//              per page x kv head x 64 dims), into a 3-stage ring.
 //   warp 1     allocates TMEM (S double buffer: 2 x 128 columns; O: d columns) and, from one
 //              thread, issues   S = Q . K^T   (M 128, N 128, K d)   and
 //                               O += P . V    (M 128, N d,   K 128)  as tcgen05.mma kind::f16,
 //              bf16 operands from shared memory (Q, K, P K-major; V read as it lands, an
 //              MN-major operand), fp32 accumulators in TMEM, completion signalled with
 //              tcgen05.commit on mbarriers.
-//   warps 2-3  warp 2 loads the V tiles the same way into their own 2-stage ring (so a K load
-//              never waits for a V stage); both release each V tile to the MMA, in an item's
-//              last tile after zeroing the rows of keys past the visible range (unloaded or
-//              past the context: 0 * NaN would poison O).
+//   warp 3     loads the V tiles the same way into their own 2-stage ring, so neither ring
+//              waits for the other.
+//   warp 2     releases each V tile to the MMA, in an item's last tile after zeroing the rows
+//              of keys past the visible range (unloaded or past the context: 0 * NaN would
+//              poison O).
 //   warps 4-7  softmax: thread = query row.  Reads its S row from TMEM, masks by select,
 //              keeps a running max m and sum l in the log2 domain and writes P (bf16) to
 //              shared memory.  O in TMEM is rescaled only when the row max grows by more
@@ -53,9 +54,11 @@ struct PrefillTcCfg {
   static constexpr int kKVBytes = BK * D * 2;
   static constexpr int kPBytes = BQ * BK * 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + kQBytes;       // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * kKVBytes;  // 2 stages
-  static constexpr int OFF_P = OFF_V + 2 * kKVBytes;
+  static constexpr int KST = 3;  // K ring stages: a K tile is requested two tiles ahead of its QK
+  static constexpr int VST = 2;  // V ring stages
+  static constexpr int OFF_K = OFF_Q + kQBytes;
+  static constexpr int OFF_V = OFF_K + KST * kKVBytes;
+  static constexpr int OFF_P = OFF_V + VST * kKVBytes;
   static constexpr int OFF_BAR = OFF_P + kPBytes;
   static constexpr int kSmemBytes = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -90,32 +93,37 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   const uint32_t sb = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* v_full = bars + 3;   // [2]
-  uint64_t* k_empty = bars + 5;  // [2] MMA finished reading the K stage
-  uint64_t* v_empty = bars + 7;  // [2] the P.V MMA finished reading the V stage
-  uint64_t* s_full = bars + 9;   // [2] S buffer written
-  uint64_t* s_free = bars + 11;  // [2] softmax finished reading the S buffer
-  uint64_t* vt_full = bars + 13;
-  uint64_t* p_full = bars + 14;
-  uint64_t* pv_done = bars + 15;
-  uint64_t* fin = bars + 16;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  uint64_t* k_full = bars + 1;    // [KST]
+  uint64_t* k_empty = bars + 4;   // [KST] MMA finished reading the K stage
+  uint64_t* v_full = bars + 7;    // [VST]
+  uint64_t* v_empty = bars + 9;   // [VST] the P.V MMA finished reading the V stage
+  uint64_t* s_full = bars + 11;   // [2] S buffer written
+  uint64_t* s_free = bars + 13;   // [2] softmax finished reading the S buffer
+  uint64_t* vt_full = bars + 15;  // V tile released to the MMA
+  uint64_t* p_full = bars + 16;
+  uint64_t* pv_done = bars + 17;
+  uint64_t* fin = bars + 18;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 19);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  static_assert(C::KST == 3 && C::VST == 2, "barrier layout");
   const float NEG_INF = -__int_as_float(0x7f800000);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::KST; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::VST; ++s) {
+      mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], 4);
     }
-    mbar_init(vt_full, 2);
+    mbar_init(vt_full, 1);
     mbar_init(p_full, 4);
     mbar_init(pv_done, 1);
     mbar_init(fin, 1);
@@ -127,14 +135,8 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_v)) : "memory");
   }
-  pdl_wait();  // the tile list is written by the planner kernel
-  pdl_trigger();
-  const int n_tiles = p.plan.header[3];
-  const int total = n_tiles * p.hq;
-  // A CTA whose first snake-order slot is past the item list has no item in any wave
-  // (every later slot is at least gridDim.x): it leaves before taking TMEM.  On a batch
-  // without prefill spans that is every CTA.
-  if (static_cast<int>(blockIdx.x) >= total) return;
+  // TMEM is taken while the planner still runs (this kernel starts early under programmatic
+  // dependent launch), so the allocation is off the critical path.
   if (warp == 1) {
     tc5::alloc(tmem_slot, C::TMEM_COLS);
     tc5::relinquish();
@@ -143,6 +145,17 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   __syncthreads();
   tc5::fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the tile list is written by the planner kernel
+  pdl_trigger();
+  const int n_tiles = p.plan.header[3];
+  const int total = n_tiles * p.hq;
+  // A CTA whose first snake-order slot is past the item list has no item in any wave
+  // (every later slot is at least gridDim.x): it gives TMEM back and leaves.  On a batch
+  // without prefill spans that is every CTA.
+  if (static_cast<int>(blockIdx.x) >= total) {
+    if (warp == 1) tc5::dealloc(tmem, C::TMEM_COLS);
+    return;
+  }
   const int G = p.hq / p.hkv;
   const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by the other items
 
@@ -170,30 +183,42 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
     // One K or V tile of 128 keys = 8 pages, issued by one warp (lane = page x 64-dim half):
     // 16-token pages are rows 16j..16j+15 of one block, or (8-token blocks) two boxes of 8
     // rows from two blocks, 1024 bytes apart in shared memory; a last half page past kv_end
-    // is not loaded (its block may not exist, and those keys are never used).
-    auto load_tile = [&](bool is_v, int jt, int s) {
-      constexpr int per = 8 * HALVES;
-      const int bmask = (1 << p.bs_log2) - 1;
-      const int box_rows = p.bs_log2 >= 4 ? 16 : 8;  // the tensor map's box height
-      const int pg = lane / HALVES;
-      const int half = lane - pg * HALVES;
+    // is not loaded (its block may not exist, and those keys are never used).  The block ids
+    // of a lane's page are read by fetch_blocks two tiles before load_tile uses them, so the
+    // table reads never sit between a freed stage and its refill.
+    constexpr int per = 8 * HALVES;
+    const int bmask = (1 << p.bs_log2) - 1;
+    const int box_rows = p.bs_log2 >= 4 ? 16 : 8;  // the tensor map's box height
+    const int lpg = lane / HALVES;                 // this lane's page within a tile
+    const int lhalf = lane - lpg * HALVES;
+    const int32_t* btrow = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
+    auto fetch_blocks = [&](int jt) -> int2 {
+      int2 r = make_int2(0, 0);
+      const int tok = jt * C::BK + lpg * 16;
+      if (jt < nkt && lane < per && tok < kv_end) {
+        r.x = btrow[tok >> p.bs_log2];
+        if (box_rows == 8 && tok + 8 < kv_end) r.y = btrow[(tok + 8) >> p.bs_log2];
+      }
+      return r;
+    };
+    auto load_tile = [&](bool is_v, int jt, int s, int2 blks) {
       const int npg = min(8, npages - jt * 8);
       const bool tail_half = box_rows == 8 && jt * C::BK + (npg - 1) * 16 + 8 >= kv_end;
       const uint32_t tile_bytes = static_cast<uint32_t>((npg * 2 - (tail_half ? 1 : 0)) * HALVES * 1024);
       uint64_t* bar = is_v ? &v_full[s] : &k_full[s];
       if (lane == 0) mbar_arrive_expect_tx(bar, tile_bytes);
       __syncwarp();
-      if (lane < per && pg < npg) {
-        unsigned char* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s * C::kKVBytes + half * C::kBlk + pg * 2048;
-        const int tok = jt * C::BK + pg * 16;
+      if (lane < per && lpg < npg) {
+        unsigned char* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s * C::kKVBytes + lhalf * C::kBlk + lpg * 2048;
+        const int tok = jt * C::BK + lpg * 16;
         for (int r = 0; r < 16 && tok + r < kv_end; r += box_rows) {
-          const int tr = tok + r;
-          int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (tr >> p.bs_log2)];
+          int blk = r == 0 ? blks.x : blks.y;
           if (blk < 0 || blk >= p.num_blocks) {
             raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
             blk = 0;
           }
-          tma_load_4d(dst + r * 128, is_v ? &P.tmap_v : &P.tmap_k, half * 64, h, tr & bmask, blk, bar, pol);
+          tma_load_4d(dst + r * 128, is_v ? &P.tmap_v : &P.tmap_k, lhalf * 64, h, (tok + r) & bmask, blk, bar,
+                      pol);
         }
       }
     };
@@ -206,14 +231,18 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
         __syncwarp();
         if (lane < HALVES) tma_load_3d(smem + C::OFF_Q + lane * C::kBlk, &P.tmap_q, lane * 64, hq, s0 + q0, q_full);
       }
+      int2 nb0 = fetch_blocks(0), nb1 = fetch_blocks(1);
       for (int jt = 0; jt < nkt && ok; ++jt) {
         const int f = t_glob + jt;
-        const int s = f & 1;
-        if (f >= 2) {
-          ok = warp_wait(&k_empty[s], ((f >> 1) - 1) & 1, p.err, abort_flag);
+        const int ks = f % C::KST;
+        const int2 cur = nb0;
+        nb0 = nb1;
+        nb1 = fetch_blocks(jt + 2);
+        if (f >= C::KST) {
+          ok = warp_wait(&k_empty[ks], (f / C::KST - 1) & 1, p.err, abort_flag);
           if (!ok) break;
         }
-        load_tile(false, jt, s);
+        load_tile(false, jt, ks, cur);
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------------- MMA issuer
@@ -225,7 +254,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
           if (!wait_or_abort(vt_full, fp & 1, p.err, abort_flag)) return false;
           if (!wait_or_abort(p_full, fp & 1, p.err, abort_flag)) return false;
           tc5::fence_after();
-          const uint32_t vst = sb + C::OFF_V + (fp & 1) * C::kKVBytes;
+          const uint32_t vst = sb + C::OFF_V + (fp % C::VST) * C::kKVBytes;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlk + (kk & 3) * 32;
@@ -233,13 +262,14 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
                         tc5::smem_desc_mn128(vst + kk * 2048, C::kBlk), kIdescPV, (first && kk == 0) ? 0u : 1u);
           }
           tc5::commit(pv_done);
-          tc5::commit(&v_empty[fp & 1]);
+          tc5::commit(&v_empty[fp % C::VST]);
           return true;
         };
         for (int jt = 0; jt < nkt && ok; ++jt) {
           const int f = t_glob + jt;
-          const int s = f & 1;
-          ok = wait_or_abort(&k_full[s], (f >> 1) & 1, p.err, abort_flag);
+          const int s = f & 1;  // S buffer
+          const int ks = f % C::KST;
+          ok = wait_or_abort(&k_full[ks], (f / C::KST) & 1, p.err, abort_flag);
           if (ok && f >= 2) ok = wait_or_abort(&s_free[s], ((f >> 1) - 1) & 1, p.err, abort_flag);
           if (!ok) break;
           tc5::fence_after();
@@ -247,37 +277,47 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlk + (kk & 3) * 32;
             tc5::mma_ss(tmem + 128u * s, tc5::smem_desc_k128(sb + C::OFF_Q + off),
-                        tc5::smem_desc_k128(sb + C::OFF_K + s * C::kKVBytes + off), kIdescQK, kk > 0 ? 1u : 0u);
+                        tc5::smem_desc_k128(sb + C::OFF_K + ks * C::kKVBytes + off), kIdescQK, kk > 0 ? 1u : 0u);
           }
           tc5::commit(&s_full[s]);
-          tc5::commit(&k_empty[s]);
+          tc5::commit(&k_empty[ks]);
           if (jt > 0) ok = issue_pv(f - 1, jt == 1);
         }
         if (ok) issue_pv(t_glob + nkt - 1, nkt == 1);
       }
       __syncwarp();
-    } else if (warp < 4) {
-      // ------------------------------------------------- V loads (warp 2) and release
+    } else if (warp == 3) {
+      // --------------------------------------------------------------------- V loads
+      // each V tile is requested as soon as P.V has freed its stage
+      bool ok = !*abort_flag;
+      int2 nb0 = fetch_blocks(0), nb1 = fetch_blocks(1);
+      for (int jt = 0; jt < nkt && ok; ++jt) {
+        const int f = t_glob + jt;
+        const int vs = f % C::VST;
+        const int2 cur = nb0;
+        nb0 = nb1;
+        nb1 = fetch_blocks(jt + 2);
+        if (f >= C::VST) ok = warp_wait(&v_empty[vs], (f / C::VST - 1) & 1, p.err, abort_flag);
+        if (!ok) break;
+        load_tile(true, jt, vs, cur);
+      }
+    } else if (warp == 2) {
+      // ----------------------------------------------------------------- V release
       // Tile f is released after P.V of tile f - 1 was issued and completed (pv_done), which
-      // also keeps this barrier at most one phase ahead of the MMA thread's waits.
-      const int tw = warp - 2;
+      // also keeps vt_full at most one phase ahead of the MMA thread's waits; in an item's
+      // last tile the rows of keys past the visible range are zeroed first.
       bool ok = !*abort_flag;
       for (int jt = 0; jt < nkt && ok; ++jt) {
         const int f = t_glob + jt;
-        const int s = f & 1;
-        if (tw == 0) {  // warp 2 also loads the V tiles, each as soon as P.V freed its stage
-          if (f >= 2) ok = warp_wait(&v_empty[s], ((f >> 1) - 1) & 1, p.err, abort_flag);
-          if (!ok) break;
-          load_tile(true, jt, s);
-        }
-        ok = warp_wait(&v_full[s], (f >> 1) & 1, p.err, abort_flag);
+        const int vs = f % C::VST;
+        ok = warp_wait(&v_full[vs], (f / C::VST) & 1, p.err, abort_flag);
         if (ok && f >= 1) ok = warp_wait(pv_done, (f - 1) & 1, p.err, abort_flag);
         if (!ok) break;
         const int vis = kv_end - jt * C::BK;  // keys of this tile that some row sees
         if (vis < C::BK) {
-          unsigned char* vbase = smem + C::OFF_V + s * C::kKVBytes;
+          unsigned char* vbase = smem + C::OFF_V + vs * C::kKVBytes;
           const int n16 = (C::BK - vis) * 8 * HALVES;  // 16-byte chunks to clear
-          for (int idx = tw * 32 + lane; idx < n16; idx += 64) {
+          for (int idx = lane; idx < n16; idx += 32) {
             const int hh = idx / ((C::BK - vis) * 8);
             const int rem = idx - hh * (C::BK - vis) * 8;
             *reinterpret_cast<uint4*>(vbase + hh * C::kBlk + (vis + (rem >> 3)) * 128 + ((rem & 7) << 4)) =
