@@ -336,27 +336,31 @@ def run_gpu(args, rank, world, local_rank):
     graph_ms = g0.elapsed_time(g1) / K
     del graph
 
-    # end to end through the public API with host buffers: pinned inputs -> device, step,
-    # result -> pinned host, every step
-    host_in = {
-        "q": torch.from_numpy(bt.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "k": torch.from_numpy(bt.k.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "v": torch.from_numpy(bt.v.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "pos": torch.from_numpy(bt.positions).pin_memory(),
-        "slots": torch.from_numpy(bt.slot_mapping).pin_memory(),
-        "tables": torch.from_numpy(bt.block_tables).pin_memory(),
-        "ctx": torch.from_numpy(bt.context_lens).pin_memory(),
-        "qsl": torch.from_numpy(bt.query_start_loc).pin_memory(),
-    }
-    dev_in = {"q": q, "k": k, "v": v, "pos": pos, "slots": slots, "tables": tables, "ctx": ctx, "qsl": qsl}
+    # end to end through the public API with host buffers, every step: the step's inputs,
+    # staged in one pinned host buffer, go up in one copy; the result comes back to pinned host
+    from paged_kv_gqa_14_gb300.staging import StepStaging
+
+    stg = StepStaging(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
+                      bt.block_tables.shape[1], device=dev)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    stg.host.q.copy_(bf(bt.q))
+    stg.host.k.copy_(bf(bt.k))
+    stg.host.v.copy_(bf(bt.v))
+    stg.host.positions.copy_(torch.from_numpy(bt.positions))
+    stg.host.slot_mapping.copy_(torch.from_numpy(bt.slot_mapping))
+    stg.host.block_tables.copy_(torch.from_numpy(bt.block_tables))
+    stg.host.context_lens.copy_(torch.from_numpy(bt.context_lens))
+    stg.host.query_start_loc.copy_(torch.from_numpy(bt.query_start_loc))
+    sd = stg.dev
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = stg.nbytes
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
-        for name, t in host_in.items():
-            dev_in[name].copy_(t, non_blocking=True)
-        step()
+        stg.upload(stream)
+        ops.kv_append(sd.q, sd.k, sd.v, sd.positions, sd.slot_mapping, kc, vc, bt.rope_theta)
+        ops.paged_attention(sd.q, kc, vc, sd.block_tables, sd.context_lens, sd.query_start_loc, bt.scale, out=out,
+                            workspace=ws)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
