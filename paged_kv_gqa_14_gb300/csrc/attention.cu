@@ -278,7 +278,9 @@ bool make_q_map(CUtensorMap* m, const AttnArgs& a) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.head_dim), static_cast<cuuint64_t>(a.hq),
                               static_cast<cuuint64_t>(a.num_tokens)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.q_sh) * 2, static_cast<cuuint64_t>(a.q_st) * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  // a box is the G heads of one kv head's group x P consecutive tokens x 64 dims
+  const int g = a.hq / a.hkv;
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(kTcPrefillRows / g)};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -292,6 +294,8 @@ bool make_prefill_tc_params(const AttnArgs& a, PrefillTcParams* P) {
       !make_pool_map(&P->tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, a.head_dim))
     return false;
   P->p = make_prefill_params(a);
+  P->group = a.hq / a.hkv;
+  P->prows = kTcPrefillRows / P->group;
   return true;
 }
 
@@ -307,7 +311,7 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaS
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int64_t max_items = (a.num_tokens / C::BQ + a.num_seqs + 1) * a.hq;
+  const int64_t max_items = (a.num_tokens / P.prows + a.num_seqs + 1) * a.hkv;
   const int64_t cap = device_sm_count();
   const unsigned grid = static_cast<unsigned>(max_items < cap ? max_items : cap);
   record_kernel_event(PKV_KERNEL_PREFILL, false, stream);
@@ -325,7 +329,7 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   // else mma.sync (64-row tiles)
   PrefillTcParams tcp;
   const bool use_tc = a.prefill_kernel == 2 && make_prefill_tc_params(a, &tcp);
-  const int tile_q = use_tc ? PrefillTcCfg<128>::BQ : kPrefillTileQ;
+  const int tile_q = use_tc ? kTcPrefillRows / (a.hq / a.hkv) : kPrefillTileQ;
   record_kernel_event(PKV_KERNEL_PLAN, false, stream);
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
                              static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps,
@@ -363,7 +367,7 @@ PlanSizes plan_sizes(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads, 
   s.num_q_heads = num_q_heads;
   s.head_dim = head_dim;
   s.decode_ctas = decode_ctas;
-  s.max_tiles = num_tokens / kPrefillTileQ + num_seqs + 1;
+  s.max_tiles = num_tokens / kMinPrefillTileQ + num_seqs + 1;
   s.max_slots = num_seqs + decode_ctas;
   size_t off = 0;
   s.off_header = off;

@@ -20,7 +20,9 @@ inline int block_size_log2(int64_t bs) {
   return -1;
 }
 constexpr int kDecodeWarps = 8;      // consumer warps of the decode split-K kernel
-constexpr int kPrefillTileQ = 64;    // query rows per prefill work tile
+constexpr int kPrefillTileQ = 64;    // query rows per mma.sync prefill work tile
+constexpr int kTcPrefillRows = 128;  // rows of a tcgen05 prefill tile: floor(128 / G) positions x G heads
+constexpr int kMinPrefillTileQ = kTcPrefillRows / 8;  // fewest positions per tile (G = 8): sizes the tile list
 constexpr int kMaxHeadDim = 128;
 // GQA group size from which the decode runs on the tensor cores by default.  Measured on
 // GB300: the tensor-core variant is at least as fast for every group size (0.87 vs 0.80 of

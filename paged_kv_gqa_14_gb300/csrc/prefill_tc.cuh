@@ -1,9 +1,12 @@
 // Prefill-chunk attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// Same work items and causal rule as prefill.cuh ("mini_engine" README, "What it does":
-// chunked prefill; "09 -- Mini Inference Engine (The Capstone)", "Week 3": mixed batches):
-// an item is (sequence, 128-row tile of its span, q head); row r of an n-row span sits at
-// position ctx - n + r and sees keys 0 .. ctx - n + r.
+// Same causal rule as prefill.cuh ("mini_engine" README, "What it does": chunked prefill;
+// "09 -- Mini Inference Engine (The Capstone)", "Week 3": mixed batches): row r of an n-row
+// span sits at position ctx - n + r and sees keys 0 .. ctx - n + r.  An item is (sequence,
+// tile of P = floor(128 / G) positions of its span, kv head h), and its 128-row Q tile
+// stacks the G query heads that share kv head h: tile row r is position q0 + r / G of q head
+// h G + r % G.  Every K/V tile is thus loaded once for the whole GQA group (G = 2: half the
+// K/V traffic of one item per q head); rows past G P are idle.
 //
 // Per item, one CTA of eight warps with fixed roles:
 //   warp 0     TMA producer: the Q tile once (3-D tensor map over q), then the K tiles of
@@ -38,10 +41,12 @@
 namespace pkv {
 
 struct PrefillTcParams {
-  CUtensorMap tmap_q;  // 3-D {d, Hq, T}, box {64, 1, 128}, 128B swizzle
+  CUtensorMap tmap_q;  // 3-D {d, Hq, T}, box {64, G, P}, 128B swizzle
   CUtensorMap tmap_k;  // 4-D {d, Hkv, 16, num_blocks}, box {64, 1, 16, 1}, 128B swizzle
   CUtensorMap tmap_v;
   PrefillParams p;
+  int group;  // G = Hq / Hkv
+  int prows;  // P = floor(128 / G): positions per item
 };
 
 template <int D>
@@ -148,7 +153,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   pdl_wait();  // the tile list is written by the planner kernel
   pdl_trigger();
   const int n_tiles = p.plan.header[3];
-  const int total = n_tiles * p.hq;
+  const int total = n_tiles * p.hkv;
   // A CTA whose first snake-order slot is past the item list has no item in any wave
   // (every later slot is at least gridDim.x): it gives TMEM back and leaves.  On a batch
   // without prefill spans that is every CTA.
@@ -156,7 +161,8 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
     if (warp == 1) tc5::dealloc(tmem, C::TMEM_COLS);
     return;
   }
-  const int G = p.hq / p.hkv;
+  const int G = P.group;
+  const int PR = P.prows;
   const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by the other items
 
   int t_glob = 0;  // K/V tiles this CTA has processed (ring slots, S buffers, PV phases)
@@ -165,16 +171,15 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
     const int ord = snake_order(wave, blockIdx.x, gridDim.x);
     if (ord >= total) continue;
     const int item = total - 1 - ord;  // later (longer) tiles of each span first
-    const int ti = item / p.hq;
-    const int hq = item - ti * p.hq;
-    const int h = hq / G;
+    const int ti = item / p.hkv;
+    const int h = item - ti * p.hkv;  // kv head; q heads h G .. h G + G - 1
     const int b = p.plan.pf_seq[ti];
     const int j = p.plan.pf_tile[ti];
     const int s0 = p.qsl[b];
     const int n = p.qsl[b + 1] - s0;
     const int ctx = p.context_lens[b];
-    const int q0 = j * C::BQ;
-    const int qrows = min(C::BQ, n - q0);
+    const int q0 = j * PR;
+    const int qrows = min(PR, n - q0);  // positions of this item
     const int pos0 = ctx - n + q0;
     const int kv_end = pos0 + qrows;  // keys [0, kv_end) are visible to some row
     const int nkt = ceil_div(kv_end, C::BK);
@@ -227,9 +232,10 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
       // ---------------------------------------------------------- TMA producer: Q and K
       bool ok = !*abort_flag;
       if (ok) {
-        if (lane == 0) mbar_arrive_expect_tx(q_full, C::kQBytes);
+        if (lane == 0) mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(HALVES * G * PR * 128));
         __syncwarp();
-        if (lane < HALVES) tma_load_3d(smem + C::OFF_Q + lane * C::kBlk, &P.tmap_q, lane * 64, hq, s0 + q0, q_full);
+        if (lane < HALVES)
+          tma_load_3d(smem + C::OFF_Q + lane * C::kBlk, &P.tmap_q, lane * 64, h * G, s0 + q0, q_full);
       }
       int2 nb0 = fetch_blocks(0), nb1 = fetch_blocks(1);
       for (int jt = 0; jt < nkt && ok; ++jt) {
@@ -332,8 +338,10 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
       // -------------------------------------------------------------------- softmax
       const int sw = warp - 4;  // TMEM lanes 32*sw .. 32*sw+31
       const int r = 32 * sw + lane;
-      const bool live = r < qrows;
-      const int pos = pos0 + r;
+      const int rt = r / G;          // position within the item
+      const int rg = r - rt * G;     // q head within the group
+      const bool live = rt < qrows;  // (rt < qrows implies r < G P)
+      const int pos = pos0 + rt;
       const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sw) << 16);
       float m_run = NEG_INF, l_run = 0.f;
       bool ok = !*abort_flag;
@@ -432,7 +440,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
       if (ok) {
         tc5::fence_after();
         const float inv = live ? 1.f / l_run : 0.f;
-        bf16* orow = p.out + static_cast<int64_t>(s0 + q0 + r) * p.o_st + static_cast<int64_t>(hq) * p.o_sh;
+        bf16* orow = p.out + static_cast<int64_t>(s0 + q0 + rt) * p.o_st + static_cast<int64_t>(h * G + rg) * p.o_sh;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];

@@ -115,6 +115,22 @@ def test_both_prefill_kernels_on_long_chunks(prefill_kernel, case):
     assert_close(got, ref, f"prefill={prefill_kernel} ctx={ctx} spans={spans}")
 
 
+@pytest.mark.parametrize("prefill_kernel", ["tcgen05"], indirect=True)
+@pytest.mark.parametrize("group", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_tcgen05_prefill_every_group_size(prefill_kernel, group, d):
+    # the tcgen05 tile stacks the G q heads of a kv head (floor(128 / G) positions x G rows):
+    # every G, ragged tiles at both ends of a chunk, a second kv head, a decode row mixed in
+    ctx, spans = [431, 150, 77], [301, 150, 1]
+    pages = sum(-(-c // 16) for c in ctx)
+    bt = W.make_batch(ctx, spans, 2 * group, 2, d, pages + 3, seed=70 + group)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert_close(got, ref, f"G={group} d={d}")
+
+
 @pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
 @pytest.mark.parametrize("seed", range(200, 210))
 def test_both_prefill_kernels_random_mixed(seed, prefill_kernel):

@@ -59,5 +59,6 @@ def test_planner_counts_match_oracle_classification(index, prefill):
     finally:
         ops.set_decode_ctas(0)
         ops.set_prefill_kernel("auto")
-    tile_q = 128 if prefill == "tcgen05" else 64
+    # tcgen05 tiles stack the G q heads of a kv head: floor(128 / G) positions per tile
+    tile_q = 128 // (bt.num_q_heads // bt.num_kv_heads) if prefill == "tcgen05" else 64
     assert header == _expected(bt, ctas, tile_q)
