@@ -322,6 +322,24 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaS
 
 }  // namespace
 
+// The pool viewed head-major for the decode, {d, block_size, Hkv, num_blocks} with strides
+// (a row, a head, a block); a box is 64 dims x min(block_size, 16) rows x all kv heads of one
+// block, 128-byte swizzled, landing as [kv head][rows][128 bytes].
+bool make_pool_map_heads(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t bs = cuuint64_t(1) << bs_log2;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), bs, static_cast<cuuint64_t>(hkv),
+                              static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(hkv) * D * 2, static_cast<cuuint64_t>(D) * 2,
+                                 bs * hkv * D * 2};
+  const cuuint32_t box[4] = {64, bs < 16 ? static_cast<cuuint32_t>(bs) : 16u, static_cast<cuuint32_t>(hkv), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_tokens == 0) return cudaSuccess;
   const int pps = kDecodeWarps / a.hkv;

@@ -32,8 +32,8 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
     configured[dev] = true;
   }
   DecodeTcParams P;
-  if (!make_pool_map(&P.tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, D) ||
-      !make_pool_map(&P.tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, D))
+  if (!make_pool_map_heads(&P.tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, D) ||
+      !make_pool_map_heads(&P.tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, D))
     return cudaErrorInvalidValue;
   DecodeParams& p = P.p;
   p.q = static_cast<const bf16*>(a.q);

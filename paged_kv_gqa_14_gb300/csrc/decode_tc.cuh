@@ -14,12 +14,14 @@
 // QK^T and 16 tokens for PV.  This removes the G-proportional CUDA-core work (G FMAs per
 // loaded element plus shuffle reductions) that caps the scalar kernel at large G.
 //
-// K/V pages are staged by 4-D TMA tensor loads (tensor map over the pool viewed as
-// [num_blocks][block_size][Hkv][d]) in boxes of 16 tokens x 64 dims of one kv head with the
-// 128-byte swizzle, so the ldmatrix reads of 8 token rows hit 8 different bank groups.  A
+// K/V pages are staged by 4-D TMA tensor loads over the pool viewed head-major,
+// {d, block rows, Hkv, num_blocks} (strides: a row, a head, a block): one box is 64 dims x
+// 16 token rows x all kv heads of a page, landing as [kv head][16 rows][128 bytes] with the
+// 128-byte swizzle, so the ldmatrix reads of 8 token rows of one head hit 8 different bank
+// groups.  One box per (page, 64-dim half) instead of one per kv head: on GB300 per-head
+// boxes of 2 KB moved 4.6 TB/s from HBM in a copy-only test, page-wide boxes 6.1 TB/s.  A
 // 16-token page is rows 16j..16j+15 of one block when blocks hold 16 or more tokens; with
-// 8-token blocks it is two boxes of 8 rows from two blocks, landing 1024 bytes apart, which
-// with the 128-byte swizzle is the same shared-memory image as one 16-row box.
+// 8-token blocks it is two boxes of 8 rows from two blocks, [row half][kv head][8 rows].
 //
 // The kernel is instantiated per block size, with it folded in at compile time.  The decode
 // is sensitive to the producer warp's instruction stream (the warp shares a scheduler with
@@ -35,7 +37,7 @@
 namespace pkv {
 
 struct DecodeTcParams {
-  CUtensorMap tmap_k;  // 4-D: {d, Hkv, block_size, num_blocks}, box {64, 1, min(block_size, 16), 1}, 128B swizzle
+  CUtensorMap tmap_k;  // 4-D: {d, block_size, Hkv, num_blocks}, box {64, min(block_size, 16), Hkv, 1}, 128B swizzle
   CUtensorMap tmap_v;
   DecodeParams p;
 };
@@ -93,8 +95,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// byte offset of 16-byte chunk `c` (0..7) of token row `t` inside a 128B-swizzled box
-__device__ __forceinline__ uint32_t box_off(int t, int c) { return t * 128 + ((c ^ (t & 7)) << 4); }
+// byte offset of 16-byte chunk `c` (0..7) of token row `t` inside its 8-row, 1024-byte
+// 128B-swizzled atom (rows t and t + 8 sit in two atoms)
+__device__ __forceinline__ uint32_t chunk_off(int t, int c) { return (t & 7) * 128 + ((c ^ (t & 7)) << 4); }
 
 // BS: tokens per pool block, a power of two from 8 to 128.
 template <int D, int G, int BS>
@@ -145,18 +148,22 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   const int hkv = p.hkv;
   const int pps = kDecodeWarps / hkv;
   const uint32_t page_bytes = static_cast<uint32_t>(hkv * HALVES * C::kBoxBytes);
+  // shared-memory image of a stage: [K|V][page][64-dim half][kv head][16 rows][128 B]; with
+  // 8-token blocks [K|V][page][half][row half][kv head][8 rows][128 B]
+  const uint32_t hstride = static_cast<uint32_t>(hkv * C::kBoxBytes);  // one (page, half) of all heads
+  constexpr bool two_block_pages = BS == 8;
+  const uint32_t head_off = two_block_pages ? 1024u : static_cast<uint32_t>(C::kBoxBytes);  // next kv head
+  const uint32_t rowhalf_off = two_block_pages ? static_cast<uint32_t>(hkv * 1024) : 1024u;  // rows 8..15
 
   if (warp == kDecodeWarps) {
     // ------------------------------------------------------------------ producer warp
     const uint64_t pol = l2_policy_evict_first();
-    // lane -> (K or V, page, kv head, half) of the unit's boxes; 16*HALVES boxes <= 32
-    const int per_kv = kDecodeWarps * HALVES;
+    // lane -> (K or V, page, 64-dim half) of the unit's boxes; 2 P HALVES <= 32 boxes
+    const int per_kv = pps * HALVES;
     const int kv = lane / per_kv;
     const int rem = lane - kv * per_kv;
-    const int bp = rem / (hkv * HALVES);
-    const int rem2 = rem - bp * hkv * HALVES;
-    const int bh = rem2 / HALVES;
-    const int bhalf = rem2 - bh * HALVES;
+    const int bp = rem / HALVES;
+    const int bhalf = rem - bp * HALVES;
     const bool lane_has_box = lane < 2 * per_kv;
     int i = i_first;
     int ustart = dec_unit[i], unext = dec_unit[i + 1];
@@ -205,11 +212,10 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
       if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * (npg * page_bytes - (tail_half ? page_bytes / 2 : 0u)));
       __syncwarp();
       if (issue) {
-        unsigned char* dst = stages + s * C::kStageBytes + kv * C::kPartBytes +
-                             ((bp * hkv + bh) * HALVES + bhalf) * C::kBoxBytes;
+        unsigned char* dst = stages + s * C::kStageBytes + kv * C::kPartBytes + (bp * HALVES + bhalf) * hstride;
         const CUtensorMap* map = kv ? &P.tmap_v : &P.tmap_k;
-        tma_load_4d(dst, map, bhalf * 64, bh, (gp * 16) & bmask, blk, &full[s], pol);
-        if (blk2 >= 0) tma_load_4d(dst + 1024, map, bhalf * 64, bh, 0, blk2, &full[s], pol);
+        tma_load_4d(dst, map, bhalf * 64, (gp * 16) & bmask, 0, blk, &full[s], pol);
+        if (blk2 >= 0) tma_load_4d(dst + hkv * 1024, map, bhalf * 64, 0, 0, blk2, &full[s], pol);
       }
     }
     const int issued = it;
@@ -261,16 +267,17 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     const int pg = (u - ustart) * pps + pw;
     if (ok && pg < npages) {
       const int rows = min(16, ctx - pg * 16);
-      const uint32_t kbox = stage_base + s * C::kStageBytes + (pw * hkv + h) * HALVES * C::kBoxBytes;
+      const uint32_t kbox = stage_base + s * C::kStageBytes + pw * HALVES * hstride + h * head_off;
       const uint32_t vbox = kbox + C::kPartBytes;
       if (rows < 16) {
         // keys past the context: zero their V rows so 0 * (unused slot) cannot poison P.V
-        unsigned char* vgen = stages + s * C::kStageBytes + C::kPartBytes + (pw * hkv + h) * HALVES * C::kBoxBytes;
+        unsigned char* vgen = stages + s * C::kStageBytes + C::kPartBytes + pw * HALVES * hstride + h * head_off;
         for (int idx = lane; idx < (16 - rows) * 8 * HALVES; idx += 32) {
           const int hh = idx / ((16 - rows) * 8);
           const int r2 = idx - hh * (16 - rows) * 8;
           const int t = rows + (r2 >> 3);
-          *reinterpret_cast<uint4*>(vgen + hh * C::kBoxBytes + t * 128 + ((r2 & 7) << 4)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vgen + hh * hstride + (t >> 3) * rowhalf_off + (t & 7) * 128 + ((r2 & 7) << 4)) =
+              make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -279,11 +286,12 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
       {
         const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const uint32_t rsel = (r >> 3) * rowhalf_off;
         const int csel = lane >> 4;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           uint32_t a[4];
-          ldsm_x4_tc(a, kbox + (kk >> 2) * C::kBoxBytes + box_off(r, 2 * (kk & 3) + csel));
+          ldsm_x4_tc(a, kbox + (kk >> 2) * hstride + rsel + chunk_off(r, 2 * (kk & 3) + csel));
           mma_16816(sc, a, qb[kk][0], qb[kk][1]);
         }
       }
@@ -322,11 +330,12 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
       // O^T += V^T . P^T
       {
         const int r = (lane & 7) + 8 * (lane >> 4);
+        const uint32_t rsel = (r >> 3) * rowhalf_off;
         const int csel = (lane >> 3) & 1;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           uint32_t a[4];
-          ldsm_x4_t_tc(a, vbox + (mt >> 2) * C::kBoxBytes + box_off(r, 2 * (mt & 3) + csel));
+          ldsm_x4_t_tc(a, vbox + (mt >> 2) * hstride + rsel + chunk_off(r, 2 * (mt & 3) + csel));
           mma_16816(acc[mt], a, pb0, pb1);
         }
       }
@@ -405,5 +414,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
 // The pool [num_blocks][block_size][Hkv][d] as a 4-D tensor map for the tensor-core
 // kernels (defined in attention.cu).
 bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D);
+// The same pool viewed head-major (page-wide boxes of all kv heads), for the decode.
+bool make_pool_map_heads(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D);
 
 }  // namespace pkv
