@@ -39,8 +39,8 @@ EncodeTiledFn encode_tiled() {
 }
 
 // The pool [num_blocks][block_size][Hkv][d] as a 4-D tensor {d, Hkv, block_size, num_blocks};
-// a box is min(block_size, 16) token rows x 64 dims of one kv head in one block, 128-byte
-// swizzled.
+// a box is all block_size token rows x 64 dims of one kv head in one block, 128-byte swizzled
+// (the tcgen05 prefill's K/V tiles).
 bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
@@ -49,7 +49,7 @@ bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_
                               static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hkv) * D * 2,
                                  bs * hkv * D * 2};
-  const cuuint32_t box[4] = {64, 1, bs < 16 ? static_cast<cuuint32_t>(bs) : 16u, 1};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(bs), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -10,8 +10,8 @@
 //
 // Per item, one CTA of eight warps with fixed roles:
 //   warp 0     TMA producer: the Q tile once (3-D tensor map over q), then the K tiles of
-//              128 keys = 8 pages gathered through the block table (4-D pool map, one box
-//              per page x kv head x 64 dims), into a 3-stage ring.
+//              128 keys gathered through the block table (4-D pool map, one box per block
+//              of the tile x 64 dims of kv head h), into a 3-stage ring.
 //   warp 1     allocates TMEM (S double buffer: 2 x 128 columns; O: d columns) and, from one
 //              thread, issues   S = Q . K^T   (M 128, N 128, K d)   and
 //                               O += P . V    (M 128, N d,   K 128)  as tcgen05.mma kind::f16,
@@ -42,7 +42,7 @@ namespace pkv {
 
 struct PrefillTcParams {
   CUtensorMap tmap_q;  // 3-D {d, Hq, T}, box {64, G, P}, 128B swizzle
-  CUtensorMap tmap_k;  // 4-D {d, Hkv, 16, num_blocks}, box {64, 1, 16, 1}, 128B swizzle
+  CUtensorMap tmap_k;  // 4-D {d, Hkv, block_size, num_blocks}, box {64, 1, block_size, 1}, 128B swizzle
   CUtensorMap tmap_v;
   PrefillParams p;
   int group;  // G = Hq / Hkv
@@ -183,48 +183,34 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
     const int pos0 = ctx - n + q0;
     const int kv_end = pos0 + qrows;  // keys [0, kv_end) are visible to some row
     const int nkt = ceil_div(kv_end, C::BK);
-    const int npages = ceil_div(kv_end, 16);
 
-    // One K or V tile of 128 keys = 8 pages, issued by one warp (lane = page x 64-dim half):
-    // 16-token pages are rows 16j..16j+15 of one block, or (8-token blocks) two boxes of 8
-    // rows from two blocks, 1024 bytes apart in shared memory; a last half page past kv_end
-    // is not loaded (its block may not exist, and those keys are never used).  The block ids
-    // of a lane's page are read by fetch_blocks two tiles before load_tile uses them, so the
-    // table reads never sit between a freed stage and its refill.
-    constexpr int per = 8 * HALVES;
-    const int bmask = (1 << p.bs_log2) - 1;
-    const int box_rows = p.bs_log2 >= 4 ? 16 : 8;  // the tensor map's box height
-    const int lpg = lane / HALVES;                 // this lane's page within a tile
-    const int lhalf = lane - lpg * HALVES;
+    // One K or V tile of 128 keys, issued by one warp: 128 / bs boxes of one whole block
+    // (bs = block_size rows; 128 is a multiple of every block size) of kv head h per 64-dim
+    // half, lane = box x half.  A box past kv_end is not loaded (its block may not exist, and
+    // those keys are never used).  Larger blocks mean fewer, taller boxes.  The block id of a
+    // lane's box is read by fetch_block two tiles before load_tile uses it, so the table reads
+    // never sit between a freed stage and its refill.
+    const int bs = 1 << p.bs_log2;
+    const int lbox = lane / HALVES;  // this lane's box within a tile
+    const int lhalf = lane - lbox * HALVES;
+    const bool lane_loads = lbox < C::BK / bs;
     const int32_t* btrow = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
-    auto fetch_blocks = [&](int jt) -> int2 {
-      int2 r = make_int2(0, 0);
-      const int tok = jt * C::BK + lpg * 16;
-      if (jt < nkt && lane < per && tok < kv_end) {
-        r.x = btrow[tok >> p.bs_log2];
-        if (box_rows == 8 && tok + 8 < kv_end) r.y = btrow[(tok + 8) >> p.bs_log2];
-      }
-      return r;
+    auto fetch_block = [&](int jt) -> int {
+      const int key0 = jt * C::BK + lbox * bs;
+      return (jt < nkt && lane_loads && key0 < kv_end) ? btrow[key0 >> p.bs_log2] : 0;
     };
-    auto load_tile = [&](bool is_v, int jt, int s, int2 blks) {
-      const int npg = min(8, npages - jt * 8);
-      const bool tail_half = box_rows == 8 && jt * C::BK + (npg - 1) * 16 + 8 >= kv_end;
-      const uint32_t tile_bytes = static_cast<uint32_t>((npg * 2 - (tail_half ? 1 : 0)) * HALVES * 1024);
+    auto load_tile = [&](bool is_v, int jt, int s, int blk) {
+      const int nbox = ceil_div(min(C::BK, kv_end - jt * C::BK), bs);
       uint64_t* bar = is_v ? &v_full[s] : &k_full[s];
-      if (lane == 0) mbar_arrive_expect_tx(bar, tile_bytes);
+      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox * bs * 128 * HALVES));
       __syncwarp();
-      if (lane < per && lpg < npg) {
-        unsigned char* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s * C::kKVBytes + lhalf * C::kBlk + lpg * 2048;
-        const int tok = jt * C::BK + lpg * 16;
-        for (int r = 0; r < 16 && tok + r < kv_end; r += box_rows) {
-          int blk = r == 0 ? blks.x : blks.y;
-          if (blk < 0 || blk >= p.num_blocks) {
-            raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
-            blk = 0;
-          }
-          tma_load_4d(dst + r * 128, is_v ? &P.tmap_v : &P.tmap_k, lhalf * 64, h, (tok + r) & bmask, blk, bar,
-                      pol);
+      if (lane_loads && lbox < nbox) {
+        if (blk < 0 || blk >= p.num_blocks) {
+          raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+          blk = 0;
         }
+        unsigned char* dst = smem + (is_v ? C::OFF_V : C::OFF_K) + s * C::kKVBytes + lhalf * C::kBlk + lbox * bs * 128;
+        tma_load_4d(dst, is_v ? &P.tmap_v : &P.tmap_k, lhalf * 64, h, 0, blk, bar, pol);
       }
     };
 
@@ -237,13 +223,13 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
         if (lane < HALVES)
           tma_load_3d(smem + C::OFF_Q + lane * C::kBlk, &P.tmap_q, lane * 64, h * G, s0 + q0, q_full);
       }
-      int2 nb0 = fetch_blocks(0), nb1 = fetch_blocks(1);
+      int nb0 = fetch_block(0), nb1 = fetch_block(1);
       for (int jt = 0; jt < nkt && ok; ++jt) {
         const int f = t_glob + jt;
         const int ks = f % C::KST;
-        const int2 cur = nb0;
+        const int cur = nb0;
         nb0 = nb1;
-        nb1 = fetch_blocks(jt + 2);
+        nb1 = fetch_block(jt + 2);
         if (f >= C::KST) {
           ok = warp_wait(&k_empty[ks], (f / C::KST - 1) & 1, p.err, abort_flag);
           if (!ok) break;
@@ -296,13 +282,13 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
       // --------------------------------------------------------------------- V loads
       // each V tile is requested as soon as P.V has freed its stage
       bool ok = !*abort_flag;
-      int2 nb0 = fetch_blocks(0), nb1 = fetch_blocks(1);
+      int nb0 = fetch_block(0), nb1 = fetch_block(1);
       for (int jt = 0; jt < nkt && ok; ++jt) {
         const int f = t_glob + jt;
         const int vs = f % C::VST;
-        const int2 cur = nb0;
+        const int cur = nb0;
         nb0 = nb1;
-        nb1 = fetch_blocks(jt + 2);
+        nb1 = fetch_block(jt + 2);
         if (f >= C::VST) ok = warp_wait(&v_empty[vs], (f / C::VST - 1) & 1, p.err, abort_flag);
         if (!ok) break;
         load_tile(true, jt, vs, cur);
