@@ -12,20 +12,20 @@
 //   warp 0     TMA producer: the Q tile once (3-D tensor map over q), then the K tiles of
 //              128 keys gathered through the block table (4-D pool map, one box per block
 //              of the tile x 64 dims of kv head h), into a 3-stage ring.
-//   warp 1     allocates TMEM (S double buffer: 2 x 128 columns; O: d columns) and, from one
+//   warp 1     allocates TMEM (S: 2 x 128 columns; O: d columns; P: 2 x 64 columns) and, from one
 //              thread, issues   S = Q . K^T   (M 128, N 128, K d)   and
 //                               O += P . V    (M 128, N d,   K 128)  as tcgen05.mma kind::f16,
-//              bf16 operands from shared memory (Q, K, P K-major; V read as it lands, an
-//              MN-major operand), fp32 accumulators in TMEM, completion signalled with
-//              tcgen05.commit on mbarriers.
+//              S from Q and K in shared memory (K-major), O from P in TMEM and V in shared
+//              memory (read as it lands, an MN-major operand), fp32 accumulators in TMEM,
+//              completion signalled with tcgen05.commit on mbarriers.
 //   warp 3     loads the V tiles the same way into their own 2-stage ring, so neither ring
 //              waits for the other.
 //   warp 2     releases each V tile to the MMA, in an item's last tile after zeroing the rows
 //              of keys past the visible range (unloaded or past the context: 0 * NaN would
 //              poison O).
 //   warps 4-7  softmax: thread = query row.  Reads its S row from TMEM, masks by select,
-//              keeps a running max m and sum l in the log2 domain and writes P (bf16) to
-//              shared memory.  O in TMEM is rescaled only when the row max grows by more
+//              keeps a running max m and sum l in the log2 domain and writes P (bf16) back to
+//              TMEM, double-buffered, so P of tile f + 1 never waits for P.V of tile f.  O in TMEM is rescaled only when the row max grows by more
 //              than 2^8 (the stale max stays the reference otherwise; O and l share it, so the
 //              result is unchanged).  At the end it reads O, divides by l and stores bf16.
 // Every wait is bounded; a CTA that times out sets PKV_DEVERR_TIMEOUT and finishes its items
@@ -57,17 +57,17 @@ struct PrefillTcCfg {
   static constexpr int kBlk = 128 * 128;  // one [128 rows][64 elements] swizzled block: 16 KB
   static constexpr int kQBytes = BQ * D * 2;
   static constexpr int kKVBytes = BK * D * 2;
-  static constexpr int kPBytes = BQ * BK * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int KST = 3;  // K ring stages: a K tile is requested two tiles ahead of its QK
-  static constexpr int VST = 2;  // V ring stages
+  static constexpr int VST = 3;  // V ring stages
   static constexpr int OFF_K = OFF_Q + kQBytes;
   static constexpr int OFF_V = OFF_K + KST * kKVBytes;
-  static constexpr int OFF_P = OFF_V + VST * kKVBytes;
-  static constexpr int OFF_BAR = OFF_P + kPBytes;
+  static constexpr int OFF_BAR = OFF_V + VST * kKVBytes;
   static constexpr int kSmemBytes = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = 256;
+  static constexpr uint32_t COL_O = 256;  // O: D columns
+  static constexpr uint32_t COL_P = 384;  // P (bf16 pairs): 2 buffers x 64 columns
+  static_assert(D <= 128, "TMEM columns: S 2 x 128, O D, P 2 x 64");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -101,16 +101,18 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   uint64_t* k_full = bars + 1;    // [KST]
   uint64_t* k_empty = bars + 4;   // [KST] MMA finished reading the K stage
   uint64_t* v_full = bars + 7;    // [VST]
-  uint64_t* v_empty = bars + 9;   // [VST] the P.V MMA finished reading the V stage
-  uint64_t* s_full = bars + 11;   // [2] S buffer written
-  uint64_t* s_free = bars + 13;   // [2] softmax finished reading the S buffer
-  uint64_t* vt_full = bars + 15;  // V tile released to the MMA
-  uint64_t* p_full = bars + 16;
-  uint64_t* pv_done = bars + 17;
-  uint64_t* fin = bars + 18;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 19);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
-  static_assert(C::KST == 3 && C::VST == 2, "barrier layout");
+  uint64_t* v_empty = bars + 10;  // [VST] the P.V MMA finished reading the V stage
+  uint64_t* s_full = bars + 13;   // [2] S buffer written
+  uint64_t* s_free = bars + 15;   // [2] softmax finished reading the S buffer
+  uint64_t* vt_full = bars + 17;  // V tile released to the MMA
+  uint64_t* p_full = bars + 18;   // [2] P buffer written
+  uint64_t* pv_done = bars + 20;  // [2] P.V of the tile whose P is in that buffer completed
+  uint64_t* fin = bars + 22;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 23);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+  static_assert(C::KST == 3 && C::VST == 3, "barrier layout");
+  // P.V of tile t completes pv_done[t % 2] for the (t / 2)-th time
+  auto pv_wait = [&](int t) { return warp_wait(&pv_done[t & 1], (t >> 1) & 1, p.err, abort_flag); };
   const float NEG_INF = -__int_as_float(0x7f800000);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -129,8 +131,10 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
       mbar_init(&s_free[s], 4);
     }
     mbar_init(vt_full, 1);
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&p_full[s], 4);
+      mbar_init(&pv_done[s], 1);
+    }
     mbar_init(fin, 1);
     fence_mbar_init();
     *abort_flag = 0;
@@ -244,16 +248,14 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
         bool ok = wait_or_abort(q_full, item_no & 1, p.err, abort_flag);
         auto issue_pv = [&](int fp, bool first) -> bool {
           if (!wait_or_abort(vt_full, fp & 1, p.err, abort_flag)) return false;
-          if (!wait_or_abort(p_full, fp & 1, p.err, abort_flag)) return false;
+          if (!wait_or_abort(&p_full[fp & 1], (fp >> 1) & 1, p.err, abort_flag)) return false;
           tc5::fence_after();
           const uint32_t vst = sb + C::OFF_V + (fp % C::VST) * C::kKVBytes;
 #pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBlk + (kk & 3) * 32;
-            tc5::mma_ss(tmem + C::COL_O, tc5::smem_desc_k128(sb + C::OFF_P + off),
+          for (int kk = 0; kk < C::BK / 16; ++kk)  // A = P from TMEM: 16 keys = 8 columns
+            tc5::mma_ts(tmem + C::COL_O, tmem + C::COL_P + 64u * (fp & 1) + 8u * kk,
                         tc5::smem_desc_mn128(vst + kk * 2048, C::kBlk), kIdescPV, (first && kk == 0) ? 0u : 1u);
-          }
-          tc5::commit(pv_done);
+          tc5::commit(&pv_done[fp & 1]);
           tc5::commit(&v_empty[fp % C::VST]);
           return true;
         };
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
         const int f = t_glob + jt;
         const int vs = f % C::VST;
         ok = warp_wait(&v_full[vs], (f / C::VST) & 1, p.err, abort_flag);
-        if (ok && f >= 1) ok = warp_wait(pv_done, (f - 1) & 1, p.err, abort_flag);
+        if (ok && f >= 1) ok = pv_wait(f - 1);
         if (!ok) break;
         const int vis = kv_end - jt * C::BK;  // keys of this tile that some row sees
         if (vis < C::BK) {
@@ -390,39 +392,41 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
         }
         const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
         l_run = l_run * corr + lsum;
-        if (jt > 0) {
-          ok = warp_wait(pv_done, (f - 1) & 1, p.err, abort_flag);  // P buffer free, O stable
+        if (jt > 0 && __any_sync(0xffffffffu, resc)) {
+          // O is rescaled only once every P.V issued so far has landed in it
+          ok = pv_wait(f - 1);
           if (!ok) break;
           tc5::fence_after();
-          if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              float o[32];
-              tc5::ld32(trow + C::COL_O + 32u * c, o);
-              tc5::wait_ld();
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tc5::ld32(trow + C::COL_O + 32u * c, o);
+            tc5::wait_ld();
 #pragma unroll
-              for (int x = 0; x < 32; ++x) o[x] *= corr;
-              tc5::st32(trow + C::COL_O + 32u * c, o);
-            }
-            tc5::wait_st();
+            for (int x = 0; x < 32; ++x) o[x] *= corr;
+            tc5::st32(trow + C::COL_O + 32u * c, o);
           }
+          tc5::wait_st();
         }
-        unsigned char* prow = smem + C::OFF_P + r * 128;
+        if (f >= 2) {  // this P buffer was read by the P.V of tile f - 2
+          ok = pv_wait(f - 2);
+          if (!ok) break;
+          tc5::fence_after();
+        }
+        // P row as bf16 pairs into TMEM, the A operand of P.V: column c holds keys 2c, 2c + 1
 #pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16) {
-          uint4 u;
-          u.x = pack_bf16x2(sc[8 * c16 + 0], sc[8 * c16 + 1]);
-          u.y = pack_bf16x2(sc[8 * c16 + 2], sc[8 * c16 + 3]);
-          u.z = pack_bf16x2(sc[8 * c16 + 4], sc[8 * c16 + 5]);
-          u.w = pack_bf16x2(sc[8 * c16 + 6], sc[8 * c16 + 7]);
-          *reinterpret_cast<uint4*>(prow + (c16 >> 3) * C::kBlk + (((c16 & 7) ^ (r & 7)) << 4)) = u;
+        for (int c = 0; c < 2; ++c) {
+          float pk[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) pk[x] = __uint_as_float(pack_bf16x2(sc[64 * c + 2 * x], sc[64 * c + 2 * x + 1]));
+          tc5::st32(trow + C::COL_P + 64u * (f & 1) + 32u * c, pk);
         }
-        fence_proxy_async_smem();
+        tc5::wait_st();
         tc5::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(&p_full[f & 1]);
       }
-      if (ok) ok = warp_wait(pv_done, (t_glob + nkt - 1) & 1, p.err, abort_flag);
+      if (ok) ok = pv_wait(t_glob + nkt - 1);
       if (ok) {
         tc5::fence_after();
         const float inv = live ? 1.f / l_run : 0.f;
