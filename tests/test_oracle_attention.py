@@ -239,3 +239,44 @@ def test_uncovered_rows_stay_nan():
     qsl = np.array([0, 1, 1], dtype=np.int32)
     out = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, qsl, bt.scale)
     assert np.all(np.isfinite(out[0])) and np.all(np.isnan(out[1]))
+
+
+@pytest.mark.parametrize("bs", [8, 32, 64, 128])
+def test_block_size_does_not_change_the_result(bs):
+    # "09 -- Mini Inference Engine (The Capstone)", "Week 4": a sequence's keys are its blocks'
+    # rows in table order, so the same keys stored in blocks of another size give the same
+    # attention (exactly: the oracle gathers the same fp64 values in the same order)
+    bt = W.make_batch([1, 17, 40, 100, 130], [1, 1, 1, 37, 1], 4, 2, 16, 40, seed=3, poison=False)
+    ref = oracle.paged_attention(bt.q, bt.k_cache, bt.v_cache, bt.block_tables, bt.context_lens,
+                                 bt.query_start_loc, bt.scale)
+    rng = np.random.default_rng(bs)
+    ctx = bt.context_lens.astype(np.int64)
+    nblk = -(-ctx // bs)
+    total = int(nblk.sum()) + 2
+    perm = rng.permutation(total)
+    kc = np.full((total, bs) + bt.k_cache.shape[2:], 0x7FC0, dtype=np.uint16)  # NaN where unused
+    vc = kc.copy()
+    table = np.full((bt.num_seqs, int(nblk.max())), -1, dtype=np.int32)
+    cur = 0
+    for b in range(bt.num_seqs):
+        table[b, : nblk[b]] = perm[cur : cur + nblk[b]]
+        cur += nblk[b]
+        for j in range(int(ctx[b])):
+            kc[table[b, j // bs], j % bs] = bt.k_cache[bt.block_tables[b, j // 16], j % 16]
+            vc[table[b, j // bs], j % bs] = bt.v_cache[bt.block_tables[b, j // 16], j % 16]
+    got = oracle.paged_attention(bt.q, kc, vc, table, bt.context_lens, bt.query_start_loc, bt.scale)
+    assert np.array_equal(got, ref)
+
+
+def test_workload_block_size_variant_is_consistent():
+    # a workload rebuilt over 32-token blocks: slots point into the tables, tables stay inside
+    # the pool, and the pool keeps its size in tokens
+    for bs in (8, 32):
+        bt = W.config(1, block_size=bs, poison=False)
+        base = W.config(1, poison=False)
+        assert bt.k_cache.shape[1] == bs
+        assert bt.num_blocks * bs == base.num_blocks * 16
+        for t, (pos, s) in enumerate(zip(bt.positions, bt.slot_mapping)):
+            b = int(np.searchsorted(bt.query_start_loc, t, side="right") - 1)
+            assert s == bt.block_tables[b, pos // bs] * bs + pos % bs
+        assert bt.block_tables.max() < bt.num_blocks
