@@ -250,9 +250,10 @@ PKV_API int pkv_set_decode_kernel(int kind);
 
 /*
  * pkv_set_prefill_kernel -- choose the arithmetic of the prefill-chunk tiles for later calls:
- * 0 automatic (currently 2), 1 bf16 mma.sync tiles of 64 query rows, 2 tcgen05 tiles of 128
- * query rows (TMEM accumulators, TMA-staged operands; falls back to 1 when q's strides do
- * not admit a TMA tensor map).  Both compute the same result up to fp32 rounding.
+ * 0 automatic (currently 2), 1 bf16 mma.sync tiles of 64 query rows of one q head, 2 tcgen05
+ * tiles of 128 rows stacking the G q heads of a kv head (floor(128 / G) positions x G heads;
+ * TMEM accumulators, TMA-staged operands; falls back to 1 when q's strides do not admit a TMA
+ * tensor map).  Both compute the same result up to fp32 rounding.
  * Process-wide; for tests and tuning.  Returns PKV_ERR_SHAPE for another value.
  */
 PKV_API int pkv_set_prefill_kernel(int kind);

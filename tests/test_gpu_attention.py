@@ -287,3 +287,18 @@ def test_cuda_graph_replay_matches_eager_step():
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), out_e.view(torch.int16))
     assert_close(out.float().cpu().numpy(), ref, "graph replay")
+
+
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
+@pytest.mark.parametrize("bs", [16, 128])
+def test_long_contexts_and_largest_group(prefill_kernel, bs):
+    # the largest shapes of the supported set: G = 8 (16 q / 2 kv heads), d 128, a 32768-token
+    # decode context, a 1000-token chunk over 19000 earlier keys, a single-key sequence
+    ctx, spans = [32768, 20000, 1], [1, 1000, 1]
+    pages = sum(-(-c // bs) for c in ctx)
+    bt = W.make_batch(ctx, spans, 16, 2, 128, pages + 4, seed=77, block_size=bs)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert_close(got, ref, f"long contexts, block size {bs}, prefill={prefill_kernel}")
