@@ -28,6 +28,25 @@ _FIELDS = (
 )
 
 
+def layout(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq):
+    """[(name, dtype, shape, byte offset, bytes)] of one step's fields, and the total bytes.
+
+    Fields are packed in ``_FIELDS`` order, each starting on a 256-byte boundary."""
+    sizes = {"T": int(num_tokens), "B": int(num_seqs), "hq": int(num_q_heads), "hkv": int(num_kv_heads),
+             "d": int(head_dim), "max_blocks": int(max_blocks_per_seq)}
+    out = []
+    off = 0
+    for name, dtype, shape_of in _FIELDS:
+        shape = shape_of(sizes)
+        n = 1
+        for x in shape:
+            n *= x
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        out.append((name, dtype, shape, off, nbytes))
+        off = (off + nbytes + _ALIGN - 1) // _ALIGN * _ALIGN
+    return out, off
+
+
 class StepStaging:
     """Pinned host and device buffers for one step's inputs, with views of each field.
 
@@ -38,23 +57,12 @@ class StepStaging:
 
     def __init__(self, num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                  device=None):
-        sizes = {"T": int(num_tokens), "B": int(num_seqs), "hq": int(num_q_heads), "hkv": int(num_kv_heads),
-                 "d": int(head_dim), "max_blocks": int(max_blocks_per_seq)}
-        layout = []
-        off = 0
-        for name, dtype, shape_of in _FIELDS:
-            shape = shape_of(sizes)
-            n = 1
-            for x in shape:
-                n *= x
-            nbytes = n * torch.empty((), dtype=dtype).element_size()
-            layout.append((name, dtype, shape, off, nbytes))
-            off = (off + nbytes + _ALIGN - 1) // _ALIGN * _ALIGN
+        fields, off = layout(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq)
         self.nbytes = off
         self._host = torch.empty(off, dtype=torch.uint8).pin_memory()
         self._dev = torch.empty(off, dtype=torch.uint8, device=device or "cuda")
-        self.host = _Views(self._host, layout)
-        self.dev = _Views(self._dev, layout)
+        self.host = _Views(self._host, fields)
+        self.dev = _Views(self._dev, fields)
 
     def upload(self, stream=None):
         """Copy the whole staged step host -> device on ``stream`` (default: current)."""
