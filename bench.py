@@ -340,8 +340,9 @@ def run_gpu(args, rank, world, local_rank):
     # staged in one pinned host buffer, go up in one copy; the result comes back to pinned host
     from paged_kv_gqa_14_gb300.staging import StepStaging
 
+    kernel_copy = args.e2e_copy == "kernel"
     stg = StepStaging(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
-                      bt.block_tables.shape[1], device=dev)
+                      bt.block_tables.shape[1], device=dev, kernel_copy=kernel_copy)
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)  # noqa: E731
     stg.host.q.copy_(bf(bt.q))
     stg.host.k.copy_(bf(bt.k))
@@ -361,7 +362,10 @@ def run_gpu(args, rank, world, local_rank):
         ops.kv_append(sd.q, sd.k, sd.v, sd.positions, sd.slot_mapping, kc, vc, bt.rope_theta)
         ops.paged_attention(sd.q, kc, vc, sd.block_tables, sd.context_lens, sd.query_start_loc, bt.scale, out=out,
                             workspace=ws)
-        host_out.copy_(out, non_blocking=True)
+        if kernel_copy:
+            ops.copy(host_out, out)
+        else:
+            host_out.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -439,6 +443,7 @@ def run_gpu(args, rank, world, local_rank):
             "ms_per_step": round(e2e_ms, 5),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
+            "copy": args.e2e_copy,
         },
         "gpu_launches": 4 * K,  # kv_append, planner, prefill tiles, decode split-K (+ merge)
         "clocks": clk,
@@ -507,6 +512,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--e2e-copy", choices=["engine", "kernel"], default="kernel",
+                    help="end-to-end leg: move the staged inputs and the output with the copy engines "
+                         "(cudaMemcpyAsync) or with a copy kernel reading/writing pinned host memory")
     ap.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32, 64, 128],
                     help="tokens per pool block (the workload keeps its pool size in tokens)")
     ap.add_argument("--seqs", type=int, default=0, help="only the first N sequences (small profiling case)")

@@ -274,6 +274,17 @@ PKV_API int pkv_set_prefill_kernel(int kind);
 PKV_API int pkv_set_kernel_events(int which, void* start_event, void* stop_event);
 
 /*
+ * pkv_copy -- copy `bytes` from `src` to `dst` with a kernel on `stream` (no function of the
+ * pages: plumbing for staging a step's inputs).  Either buffer may be device memory or pinned
+ * host memory the device can address under unified addressing (e.g. from cudaHostAlloc); on
+ * a Grace-Blackwell part the SMs reach pinned host memory over NVLink-C2C.  Ordered on
+ * `stream` like any kernel.  Both pointers and `bytes` must be multiples of 16 (else
+ * PKV_ERR_ALIGN); NULL pointers give PKV_ERR_NULL; bytes == 0 is a no-op.  The buffers must
+ * not overlap.
+ */
+PKV_API int pkv_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * pkv_get_device_error -- read the current device's error word (PKV_DEVERR_* bits or-ed
  * together since the last clear) into *bits, after synchronising `stream`.  If clear != 0
  * the word is reset to zero.  This call blocks the host; the others never do.

@@ -45,6 +45,7 @@ SIGNATURES = {
     "pkv_set_prefill_kernel": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_kernel_events": (ctypes.c_int, [ctypes.c_int, _c_p, _c_p]),
     "pkv_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _c_p]),
+    "pkv_copy": (ctypes.c_int, [_c_p, _c_p, ctypes.c_size_t, _c_p]),
 }
 
 STATUS = {

@@ -21,7 +21,7 @@ LIB = os.path.join(BUILD, "libpkv.so")
 
 # (source, object name, extra flags): decode_tc.cu is built once per pool block size
 SOURCES = [("abi.cu", "abi.o", []), ("kv_append.cu", "kv_append.o", []), ("attention.cu", "attention.o", []),
-           ("noalloc.cu", "noalloc.o", [])] + [
+           ("noalloc.cu", "noalloc.o", []), ("copy.cu", "copy.o", [])] + [
     ("decode_tc.cu", f"decode_tc_bs{bs}.o", [f"-DPKV_DECODE_TC_BS={bs}"]) for bs in (8, 16, 32, 64, 128)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No --use_fast_math: sincosf in the RoPE kernel stays the accurate library routine; the

@@ -217,3 +217,21 @@ def set_kernel_events(kernel, start=None, stop=None):
     sp = ctypes.c_void_p(start.cuda_event) if start is not None else None
     ep = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
     _lib.check("pkv_set_kernel_events", _lib.load().pkv_set_kernel_events(which, sp, ep))
+
+
+def copy(dst, src, stream=None):
+    """Byte copy src -> dst by a kernel (``pkv_copy``); either tensor may be on the device or in
+    pinned host memory.  Both must be contiguous, of equal byte size, 16-byte aligned."""
+    for name, t in (("dst", dst), ("src", src)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src differ in byte size")
+    _lib.check("pkv_copy", _lib.load().pkv_copy(dst.data_ptr(), src.data_ptr(), nbytes, _stream_ptr(stream)))
+    return dst
+

@@ -56,7 +56,8 @@ class StepStaging:
     """
 
     def __init__(self, num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                 device=None):
+                 device=None, kernel_copy=False):
+        self.kernel_copy = bool(kernel_copy)
         fields, off = layout(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq)
         self.nbytes = off
         self._host = torch.empty(off, dtype=torch.uint8).pin_memory()
@@ -65,8 +66,15 @@ class StepStaging:
         self.dev = _Views(self._dev, fields)
 
     def upload(self, stream=None):
-        """Copy the whole staged step host -> device on ``stream`` (default: current)."""
+        """Copy the whole staged step host -> device on ``stream`` (default: current): one
+        copy-engine transfer, or with ``kernel_copy`` one copy kernel reading the pinned
+        buffer directly (``ops.copy``)."""
         s = torch.cuda.current_stream() if stream is None else stream
+        if self.kernel_copy:
+            from . import ops
+
+            ops.copy(self._dev, self._host, stream=s)
+            return
         with torch.cuda.stream(s):
             self._dev.copy_(self._host, non_blocking=True)
 

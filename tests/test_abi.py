@@ -136,3 +136,12 @@ def test_library_has_no_cpu_fallback_symbols():
 def test_ctypes_signature_count_matches_header():
     assert len(declared_functions()) == len([n for n in _lib.SIGNATURES])
     assert ctypes.sizeof(ctypes.c_size_t) == 8
+
+
+def test_copy_host_validation(lib):
+    assert lib.pkv_copy(None, None, 0, None) == 0  # no-op before any check
+    assert lib.pkv_copy(None, 256, 64, None) == 1
+    assert lib.pkv_copy(256, None, 64, None) == 1
+    assert lib.pkv_copy(264, 256, 64, None) == 4  # dst not 16-byte aligned
+    assert lib.pkv_copy(256, 256, 60, None) == 4  # size not a multiple of 16
+

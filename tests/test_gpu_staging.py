@@ -50,3 +50,33 @@ def test_staged_step_matches_unstaged_step(index):
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     for name in ("positions", "slot_mapping", "block_tables", "context_lens", "query_start_loc"):
         assert torch.equal(getattr(s, name).cpu(), getattr(stg.host, name)), name
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096, 1 << 20, (3 << 20) + 48])
+def test_kernel_copy_round_trip_through_pinned_host_memory(nbytes):
+    g = torch.Generator().manual_seed(nbytes)
+    src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g).pin_memory()
+    dev = torch.full((nbytes,), 7, dtype=torch.uint8, device="cuda")
+    back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    ops.copy(dev, src)
+    ops.copy(back, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), src)
+    assert torch.equal(back, src)
+
+
+def test_staged_upload_by_kernel_equals_copy_engine():
+    bt = W.config(1)
+    a = StepStaging(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
+                    bt.block_tables.shape[1])
+    b = StepStaging(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
+                    bt.block_tables.shape[1], kernel_copy=True)
+    for st in (a, b):
+        st._host.zero_()  # fields not set below hold whatever the allocation held
+        st.host.q.copy_(_bf(bt.q))
+        st.host.block_tables.copy_(torch.from_numpy(bt.block_tables))
+        st.host.query_start_loc.copy_(torch.from_numpy(bt.query_start_loc))
+        st.upload()
+    torch.cuda.synchronize()
+    assert torch.equal(a._dev.cpu(), b._dev.cpu())
+
