@@ -232,6 +232,7 @@ def run_gpu(args, rank, world, local_rank):
         ops.set_decode_kernel(args.decode_kernel)
     if args.prefill_kernel != "auto":
         ops.set_prefill_kernel(args.prefill_kernel)
+    ops.set_overlap(not args.no_overlap)
     dev = torch.device("cuda", local_rank)
     dist = None
     if world > 1:
@@ -408,6 +409,7 @@ def run_gpu(args, rank, world, local_rank):
             "parallelism": f"replicas x{world}",
             "decode_kernel": args.decode_kernel,
             "prefill_kernel": args.prefill_kernel,
+            "prefill_beside_decode": not args.no_overlap,
             "l2": "inputs larger than L2 (unique KV per step %.0f MB > 129 MB); no flush" % (kv_u / 1e6),
         },
         "tokens_per_s_per_layer": round(world * bt.num_tokens / (ms_step * 1e-3), 1),
@@ -520,6 +522,8 @@ def main():
     ap.add_argument("--seqs", type=int, default=0, help="only the first N sequences (small profiling case)")
     ap.add_argument("--decode-kernel", choices=["auto", "simt", "tensor"], default="auto")
     ap.add_argument("--prefill-kernel", choices=["auto", "mma", "tcgen05"], default="auto")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="prefill tiles before the decode on one stream (default: beside it, SMs split)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args()

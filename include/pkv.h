@@ -183,6 +183,11 @@ PKV_API size_t pkv_paged_attention_workspace_size(int64_t num_tokens, int64_t nu
  *                    must be stream-ordered.
  * Supported: head_dim in {64, 128}; num_kv_heads in {1, 2, 4, 8};
  *            num_q_heads / num_kv_heads in [1, 8].
+ * Ordering: all work is ordered after earlier work on `stream`, and later work on `stream`
+ * is ordered after all of it.  With prefill spans (num_tokens > num_seqs) the prefill tiles
+ * may run on a second stream of the library's own, forked from `stream` after the planner
+ * and joined back into it before the call returns (pkv_set_overlap); this also holds
+ * inside a CUDA graph capture of `stream`.
  */
 PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64_t q_stride_head,
                         const void* k_cache_dev, const void* v_cache_dev,
@@ -237,6 +242,17 @@ PKV_API int pkv_paged_attention_noalloc(const void* q_dev, int64_t q_stride_toke
  * or PKV_ERR_SHAPE for a negative value.
  */
 PKV_API int pkv_set_decode_ctas(int32_t ctas);
+
+/*
+ * pkv_set_overlap -- 1 (default): a batch with prefill spans runs its prefill tiles on a
+ * second stream at the same time as the decode, the SMs split between the two by the
+ * planner (the decode is bound by HBM bandwidth and reaches it without every SM); 0: the
+ * prefill tiles and then the decode run on the caller's stream, each over all SMs.  Only
+ * the tcgen05 prefill tiles with the default decode grid (pkv_set_decode_ctas(0)) use the
+ * split.  Prefill rows are bit-identical either way; decode rows may differ by fp32
+ * rounding (other split points).  Process-wide.  Returns PKV_ERR_SHAPE for another value.
+ */
+PKV_API int pkv_set_overlap(int on);
 
 /*
  * pkv_set_decode_kernel -- choose the arithmetic of the decode split-K kernel for later calls:

@@ -41,6 +41,7 @@ SIGNATURES = {
          _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_float, _c_p],
     ),
     "pkv_set_decode_ctas": (ctypes.c_int, [ctypes.c_int32]),
+    "pkv_set_overlap": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_decode_kernel": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_prefill_kernel": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_kernel_events": (ctypes.c_int, [ctypes.c_int, _c_p, _c_p]),

@@ -21,6 +21,9 @@ int g_sm_count[kMaxDevices];
 std::atomic<int> g_decode_ctas_override{0};
 std::atomic<int> g_decode_kernel{0};
 std::atomic<int> g_prefill_kernel{0};
+std::atomic<int> g_overlap{1};
+SideStream g_side[kMaxDevices];
+std::mutex g_side_lock[kMaxDevices];
 constexpr int kNumKernels = 5;
 std::atomic<void*> g_events[kNumKernels][2];
 
@@ -39,6 +42,15 @@ bool device_setup(int dev) {
     if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) g_err_ptr[dev] = static_cast<unsigned int*>(p);
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) g_sm_count[dev] = n;
+    // the second stream for prefill tiles beside the decode, and its fork/join events
+    SideStream& sd = g_side[dev];
+    if (cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      sd.stream = nullptr;
+    }
+    sd.lock = &g_side_lock[dev];
   });
   return g_err_ptr[dev] != nullptr && g_sm_count[dev] > 0;
 }
@@ -67,6 +79,15 @@ void record_kernel_event(int which, bool after, cudaStream_t stream) {
 }
 
 int decode_kernel_choice() { return g_decode_kernel.load(); }
+
+int overlap_choice() { return g_overlap.load(); }
+
+bool side_stream_for_device(SideStream* s) {
+  const int dev = current_device();
+  if (!device_setup(dev) || g_side[dev].stream == nullptr) return false;
+  *s = g_side[dev];
+  return true;
+}
 
 // Automatic choice: the tcgen05 tiles (65 us vs 113 us for the mma.sync tiles on the
 // mixed chunked-prefill workload on GB300).
@@ -102,6 +123,12 @@ const char* pkv_status_string(int status) {
 }
 
 int pkv_version(void) { return 100; }
+
+int pkv_set_overlap(int on) {
+  if (on != 0 && on != 1) return PKV_ERR_SHAPE;
+  g_overlap.store(on);
+  return PKV_OK;
+}
 
 int pkv_set_decode_ctas(int32_t ctas) {
   if (ctas < 0) return PKV_ERR_SHAPE;
@@ -306,6 +333,7 @@ int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k
   a.decode_ctas = ctas;
   a.decode_kernel = decode_kernel_choice();
   a.prefill_kernel = prefill_kernel_choice();
+  a.overlap = overlap_choice();
   a.plan = plan_view(workspace, ps);
   a.max_tiles = ps.max_tiles;
   a.err = g_err_ptr[dev];

@@ -9,7 +9,10 @@
 //      ... and the CTA that writes the last split state of a sequence cut by a CTA boundary
 //      merges that sequence's states (the split merge runs inside the decode kernel)
 // Every kernel is launched with programmatic dependent launch, so each one's launch and
-// prologue overlap the previous kernel's tail.
+// prologue overlap the previous kernel's tail.  A batch with prefill spans instead runs
+// the prefill kernel on a second stream, forked after the planner and joined back before
+// the call returns, at the same time as the decode: the planner gives the prefill P of
+// the SMs and spreads the decode units over the rest (SplitArgs in internal.h).
 #include <mutex>
 
 #include "decode.cuh"
@@ -121,10 +124,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             int num_seqs, int64_t num_tokens,
                                                             int64_t max_ctx, int pps,
                                                             int decode_ctas, int tile_q, Plan plan,
-                                                            int64_t max_tiles, unsigned int* err) {
+                                                            int64_t max_tiles, SplitArgs split,
+                                                            unsigned int* err) {
   __shared__ int sm[3 * 32];
   __shared__ int carry[3];
-  if (threadIdx.x == 0) carry[0] = carry[1] = carry[2] = 0;
+  __shared__ unsigned long long pf_keytiles;  // 128-key tiles over all prefill q tiles (one kv head)
+  __shared__ int pf_maxtile;                  // the most key tiles of one q tile
+  __shared__ unsigned long long best;         // (cost bits << 32) | prefill CTAs
+  if (threadIdx.x == 0) {
+    carry[0] = carry[1] = carry[2] = 0;
+    pf_keytiles = 0;
+    pf_maxtile = 0;
+    best = ~0ull;
+  }
   __syncthreads();
   pdl_wait();  // the workspace may still be read by the previous call's kernels until now
   pdl_trigger();
@@ -151,7 +163,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         v.a = 1;
         v.b = ceil_div(ceil_div(ctx, kPageTokens), pps);
       }
-      if (ok && span > 1) v.c = ceil_div(span, tile_q);
+      if (ok && span > 1) {
+        v.c = ceil_div(span, tile_q);
+        if (split.on) {  // keys [0, kv_end) of q tile j are read in 128-key tiles
+          unsigned long long sum = 0;
+          int mx = 0;
+          for (int j = 0; j < v.c; ++j) {
+            const int nk = ceil_div(ctx - span + min((j + 1) * tile_q, span), 128);
+            sum += static_cast<unsigned long long>(nk);
+            mx = max(mx, nk);
+          }
+          atomicAdd(&pf_keytiles, sum);
+          atomicMax(&pf_maxtile, mx);
+        }
+      }
     }
     Int3 tot;
     Int3 ex = block_scan3(v, tot, sm);
@@ -180,7 +205,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   const int n_dec = carry[0];
   const int U = carry[1];
   const int n_tiles = static_cast<int>(min(static_cast<int64_t>(carry[2]), max_tiles));
-  const int W = max(1, ceil_div(U, decode_ctas));
+  // prefill CTAs that take items, and the decode CTAs the units are spread over
+  int pn = split.pf_grid;  // serial order: every launched prefill CTA
+  int dctas = decode_ctas;
+  if (split.on) {
+    const int64_t items = static_cast<int64_t>(n_tiles) * split.hkv;
+    int hi = static_cast<int>(min(static_cast<int64_t>(split.pf_grid), items));
+    if (U > 0) hi = min(hi, split.sms - 1);
+    if (hi <= 0) {
+      pn = 0;
+    } else if (U == 0) {
+      pn = hi;
+    } else {
+      // the share minimising max(decode time on sms - p SMs, prefill time on p SMs)
+      const float kt = static_cast<float>(pf_keytiles) * static_cast<float>(split.hkv);
+      const float dec_bytes = static_cast<float>(U) * split.unit_bytes;
+      for (int p = 1 + static_cast<int>(threadIdx.x); p <= hi; p += kPlanThreads) {
+        const float t_dec = dec_bytes / fminf(split.hbm, static_cast<float>(split.sms - p) * split.dec_sm);
+        const float t_pf = fmaxf(kt / static_cast<float>(p), static_cast<float>(pf_maxtile)) * split.tile_bytes /
+                           split.pf_sm;
+        const unsigned long long key =
+            (static_cast<unsigned long long>(__float_as_uint(fmaxf(t_dec, t_pf))) << 32) | static_cast<unsigned>(p);
+        atomicMin(&best, key);
+      }
+      __syncthreads();
+      pn = static_cast<int>(best & 0xffffffffu);
+    }
+    if (U > 0) dctas = split.sms - pn;
+  }
+  const int W = max(1, ceil_div(U, max(1, dctas)));
   if (threadIdx.x == 0) plan.dec_unit[n_dec] = U;
   __syncthreads();
 
@@ -214,6 +267,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     plan.header[2] = W;
     plan.header[3] = n_tiles;
     plan.header[4] = carry2;
+    plan.header[5] = pn;
   }
 }
 
@@ -299,8 +353,15 @@ bool make_prefill_tc_params(const AttnArgs& a, PrefillTcParams* P) {
   return true;
 }
 
+// CTAs the tcgen05 prefill is launched with: one per SM, at most one per item.
+int64_t prefill_tc_grid(const AttnArgs& a, int prows) {
+  const int64_t max_items = (a.num_tokens / prows + a.num_seqs + 1) * a.hkv;
+  const int64_t cap = device_sm_count();
+  return max_items < cap ? max_items : cap;
+}
+
 template <int D>
-cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaStream_t stream) {
+cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaStream_t stream, bool pdl) {
   using C = PrefillTcCfg<D>;
   static bool configured[64] = {};
   int dev = 0;
@@ -311,11 +372,9 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaS
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int64_t max_items = (a.num_tokens / P.prows + a.num_seqs + 1) * a.hkv;
-  const int64_t cap = device_sm_count();
-  const unsigned grid = static_cast<unsigned>(max_items < cap ? max_items : cap);
+  const unsigned grid = static_cast<unsigned>(prefill_tc_grid(a, P.prows));
   record_kernel_event(PKV_KERNEL_PREFILL, false, stream);
-  const cudaError_t e = launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(256), C::kSmemBytes, stream, P);
+  const cudaError_t e = launch_kernel(pdl, prefill_tc_kernel<D>, dim3(grid), dim3(256), C::kSmemBytes, stream, P);
   record_kernel_event(PKV_KERNEL_PREFILL, true, stream);
   return e;
 }
@@ -348,30 +407,61 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   PrefillTcParams tcp;
   const bool use_tc = a.prefill_kernel == 2 && make_prefill_tc_params(a, &tcp);
   const int tile_q = use_tc ? kTcPrefillRows / (a.hq / a.hkv) : kPrefillTileQ;
+  const int sms = device_sm_count();
+  const int64_t pf_grid = use_tc ? prefill_tc_grid(a, tcp.prows) : prefill_mma_grid(a);
+  // Prefill beside the decode: only with spans of two or more tokens (more tokens than
+  // sequences), the tcgen05 tiles (one CTA per SM) and the default one decode CTA per SM.
+  SideStream side{};
+  const bool split = a.overlap && use_tc && a.num_tokens > a.num_seqs && a.decode_ctas == sms && sms > 1 &&
+                     side_stream_for_device(&side);
+  SplitArgs sp{};
+  sp.on = split ? 1 : 0;
+  sp.sms = sms;
+  sp.pf_grid = static_cast<int>(pf_grid);
+  sp.hkv = a.hkv;
+  sp.unit_bytes = static_cast<float>(kDecodeWarps) * kPageTokens * a.head_dim * 4.f;  // pps x hkv = 8 pages of K and V
+  sp.tile_bytes = 128.f * a.head_dim * 4.f;
+  sp.hbm = kSplitHbmBytesPerNs;
+  sp.dec_sm = kSplitDecodeSmBytesPerNs;
+  sp.pf_sm = split_prefill_sm_bytes_per_ns(a.bs_log2);
   record_kernel_event(PKV_KERNEL_PLAN, false, stream);
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
                              static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps,
                              a.decode_ctas, tile_q,
-                             a.plan, a.max_tiles, a.err);
+                             a.plan, a.max_tiles, sp, a.err);
   record_kernel_event(PKV_KERNEL_PLAN, true, stream);
   if (e != cudaSuccess) return e;
-  if (use_tc)
-    e = (a.head_dim == 128) ? launch_prefill_tc<128>(a, tcp, stream) : launch_prefill_tc<64>(a, tcp, stream);
-  else
-    e = (a.head_dim == 128) ? launch_prefill<128>(a, stream) : launch_prefill<64>(a, stream);
-  if (e != cudaSuccess) return e;
-  const int kind = a.decode_kernel != 0 ? a.decode_kernel : (a.hq / a.hkv >= kTensorDecodeMinGroup ? 2 : 1);
-  if (kind == 2) {
-    switch (a.bs_log2) {  // one compiled instance per block size (decode_tc.cu)
-      case 3: return launch_decode_tc_bs8(a, stream);
-      case 4: return launch_decode_tc_bs16(a, stream);
-      case 5: return launch_decode_tc_bs32(a, stream);
-      case 6: return launch_decode_tc_bs64(a, stream);
-      case 7: return launch_decode_tc_bs128(a, stream);
-      default: return cudaErrorInvalidValue;
+  auto prefill = [&](cudaStream_t s, bool pdl) -> cudaError_t {
+    if (use_tc)
+      return (a.head_dim == 128) ? launch_prefill_tc<128>(a, tcp, s, pdl) : launch_prefill_tc<64>(a, tcp, s, pdl);
+    return (a.head_dim == 128) ? launch_prefill<128>(a, s, pdl) : launch_prefill<64>(a, s, pdl);
+  };
+  auto decode = [&]() -> cudaError_t {
+    const int kind = a.decode_kernel != 0 ? a.decode_kernel : (a.hq / a.hkv >= kTensorDecodeMinGroup ? 2 : 1);
+    if (kind == 2) {
+      switch (a.bs_log2) {  // one compiled instance per block size (decode_tc.cu)
+        case 3: return launch_decode_tc_bs8(a, stream);
+        case 4: return launch_decode_tc_bs16(a, stream);
+        case 5: return launch_decode_tc_bs32(a, stream);
+        case 6: return launch_decode_tc_bs64(a, stream);
+        case 7: return launch_decode_tc_bs128(a, stream);
+        default: return cudaErrorInvalidValue;
+      }
     }
+    return (a.head_dim == 128) ? launch_decode_g<128>(a, stream) : launch_decode_g<64>(a, stream);
+  };
+  if (!split) {
+    e = prefill(stream, true);
+    return e != cudaSuccess ? e : decode();
   }
-  return (a.head_dim == 128) ? launch_decode_g<128>(a, stream) : launch_decode_g<64>(a, stream);
+  // fork after the planner, decode here, prefill on the side stream, join before returning
+  std::lock_guard<std::mutex> hold(*static_cast<std::mutex*>(side.lock));
+  if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess) return e;
+  if ((e = decode()) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess) return e;
+  if ((e = prefill(side.stream, false)) != cudaSuccess) return e;
+  if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(stream, side.join, 0);
 }
 
 // ------------------------------------------------------------------ workspace layout

@@ -38,6 +38,7 @@ constexpr int kTensorDecodeMinGroup = 1;
 // header[2] work units per decode CTA                          W = ceil(U / C)
 // header[3] number of prefill (seq, q-tile) work items         n_tiles
 // header[4] partial-result slots in use                        S
+// header[5] prefill CTAs that take work items                  P (the rest leave at once)
 //
 // A decode work unit is one page group of one sequence: P = kDecodeWarps / Hkv
 // consecutive 16-token pages (kPageTokens), all kv heads.  Decode CTA c owns units [c W, (c+1) W) of
@@ -114,6 +115,7 @@ struct AttnArgs {
   int decode_ctas;
   int decode_kernel;   // 0 automatic, 1 CUDA-core (warp-shuffle), 2 tensor-core (mma.sync)
   int prefill_kernel;  // 1 mma.sync tiles, 2 tcgen05 tiles (resolved from the process setting)
+  int overlap;         // 1: prefill tiles run beside the decode on a second stream (SMs split)
   Plan plan;
   int64_t max_tiles;
   unsigned int* err;
@@ -128,12 +130,51 @@ cudaError_t launch_decode_tc_bs128(const AttnArgs& a, cudaStream_t stream);
 
 int device_sm_count();
 
-// Launch `kernel` on `stream` with programmatic stream serialisation (PDL): it may begin
-// while the previous kernel on the stream finishes; the kernel itself calls pdl_wait()
-// before touching anything an earlier kernel wrote.
+// ------------------------------------------------------ prefill beside the decode
+// A batch with prefill spans runs its prefill tiles on a second stream while the decode
+// runs, each kernel on its own share of the SMs: the decode is bound by HBM and reaches
+// its rate on about 120 of GB300's 152 SMs (measured: 153.9 us at 112 CTAs, 153.6 us at 152
+// on the 256-sequence batch), while the prefill tiles are bound by what each SM can take
+// in (TMA boxes of one kv head's rows).  The planner picks the prefill share P that
+// minimises max(decode time on C - P SMs, prefill time on P SMs) with this model:
+//   decode:  U units x unit bytes / min(HBM rate, SMs x per-SM decode rate)
+//   prefill: max(key tiles / P, largest item's key tiles) x tile bytes / per-SM prefill rate
+// Rates in bytes per ns (= GB/s), measured on GB300.  The split only moves work between
+// SMs: every CTA computes what it would compute in the serial order.
+constexpr float kSplitHbmBytesPerNs = 6500.f;
+constexpr float kSplitDecodeSmBytesPerNs = 58.f;
+// One TMA box of the prefill is block_size rows x 128 bytes of one kv head; small boxes
+// arrive more slowly (GB300, boxes from L2: 37 GB/s per SM at 2 KB, 65 GB/s at 16 KB).
+inline float split_prefill_sm_bytes_per_ns(int bs_log2) {
+  return bs_log2 <= 3 ? 26.f : bs_log2 == 4 ? 36.f : bs_log2 == 5 ? 48.f : 58.f;
+}
+
+struct SplitArgs {
+  int on;             // 1: the planner splits `sms` CTAs between prefill and decode
+  int sms;            // CTAs to share out (one per SM)
+  int pf_grid;        // CTAs the prefill kernel is launched with
+  int hkv;            // prefill items per q tile (one per kv head)
+  float unit_bytes;   // K/V bytes of one decode work unit
+  float tile_bytes;   // K/V bytes of one prefill key tile (128 keys of one kv head)
+  float hbm, dec_sm, pf_sm;  // bytes per ns
+};
+
+// The second stream of a device and the two events that fork it from, and join it back
+// into, the caller's stream; `lock` serialises the fork/join sequence between host threads.
+struct SideStream {
+  cudaStream_t stream;
+  cudaEvent_t fork, join;
+  void* lock;  // std::mutex
+};
+bool side_stream_for_device(SideStream* s);
+int overlap_choice();
+
+// Launch `kernel` on `stream`, with programmatic stream serialisation (PDL) when `pdl`: it
+// may then begin while the previous kernel on the stream finishes; the kernel itself calls
+// pdl_wait() before touching anything an earlier kernel wrote (a no-op without PDL).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args&&... args) {
+cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -143,8 +184,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  return launch_kernel(true, kernel, grid, block, smem, stream, static_cast<Args&&>(args)...);
 }
 
 // Records the caller's timing event around a kernel launch when one is registered

@@ -140,9 +140,13 @@ __global__ void __launch_bounds__(128) prefill_kernel(const __grid_constant__ Pr
   const int n_tiles = p.plan.header[3];
   const int total = n_tiles * p.hq;
   const int G = p.hq / p.hkv;
+  // the planner's count of CTAs that take items (fewer than launched when the prefill
+  // shares the SMs with the decode); the others leave
+  const int nact = min(max(p.plan.header[5], 0), static_cast<int>(gridDim.x));
+  if (static_cast<int>(blockIdx.x) >= nact) return;
 
-  for (int wave = 0; wave * static_cast<int>(gridDim.x) < total; ++wave) {
-    const int ord = snake_order(wave, blockIdx.x, gridDim.x);
+  for (int wave = 0; wave * nact < total; ++wave) {
+    const int ord = snake_order(wave, blockIdx.x, nact);
     if (ord >= total) continue;
     const int item = total - 1 - ord;  // later (longer) tiles of each span first
     const int ti = item / p.hq;
@@ -319,8 +323,15 @@ inline PrefillParams make_prefill_params(const AttnArgs& a) {
   return p;
 }
 
+// CTAs the mma.sync prefill is launched with: two per SM, at most one per item.
+inline int64_t prefill_mma_grid(const AttnArgs& a) {
+  const int64_t max_items = a.max_tiles * a.hq;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 2;
+  return max_items < cap ? max_items : cap;
+}
+
 template <int D>
-cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream) {
+cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream, bool pdl) {
   using C = PrefillCfg<D>;
   static bool configured[64] = {};
   int dev = 0;
@@ -332,12 +343,11 @@ cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream) {
     configured[dev] = true;
   }
   const PrefillParams p = make_prefill_params(a);
-  const int64_t max_items = a.max_tiles * a.hq;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 2;
-  const unsigned grid = static_cast<unsigned>(max_items < cap ? max_items : cap);
+  const unsigned grid = static_cast<unsigned>(prefill_mma_grid(a));
   if (grid == 0) return cudaSuccess;
   record_kernel_event(PKV_KERNEL_PREFILL, false, stream);
-  const cudaError_t e = launch_pdl(prefill_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, p);
+  const cudaError_t e =
+      launch_kernel(pdl, prefill_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, p);
   record_kernel_event(PKV_KERNEL_PREFILL, true, stream);
   return e;
 }

@@ -158,10 +158,12 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   pdl_trigger();
   const int n_tiles = p.plan.header[3];
   const int total = n_tiles * p.hkv;
-  // A CTA whose first snake-order slot is past the item list has no item in any wave
-  // (every later slot is at least gridDim.x): it gives TMEM back and leaves.  On a batch
-  // without prefill spans that is every CTA.
-  if (static_cast<int>(blockIdx.x) >= total) {
+  // CTAs that take items: the planner's count, fewer than launched when the prefill shares
+  // the SMs with the decode.  A CTA past it, or whose first snake-order slot is past the
+  // item list (every later slot is at least nact), has no item in any wave: it gives TMEM
+  // back and leaves.  On a batch without prefill spans that is every CTA.
+  const int nact = min(max(p.plan.header[5], 0), static_cast<int>(gridDim.x));
+  if (static_cast<int>(blockIdx.x) >= total || static_cast<int>(blockIdx.x) >= nact) {
     if (warp == 1) tc5::dealloc(tmem, C::TMEM_COLS);
     return;
   }
@@ -171,8 +173,8 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
 
   int t_glob = 0;  // K/V tiles this CTA has processed (ring slots, S buffers, PV phases)
   int item_no = 0;
-  for (int wave = 0; wave * static_cast<int>(gridDim.x) < total; ++wave) {
-    const int ord = snake_order(wave, blockIdx.x, gridDim.x);
+  for (int wave = 0; wave * nact < total; ++wave) {
+    const int ord = snake_order(wave, blockIdx.x, nact);
     if (ord >= total) continue;
     const int item = total - 1 - ord;  // later (longer) tiles of each span first
     const int ti = item / p.hkv;

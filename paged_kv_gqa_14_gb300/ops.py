@@ -183,6 +183,12 @@ def set_decode_ctas(n):
     _lib.check("pkv_set_decode_ctas", _lib.load().pkv_set_decode_ctas(int(n)))
 
 
+def set_overlap(on):
+    """Run a mixed batch's prefill tiles beside the decode on a second stream (True, the
+    default) or before it on the caller's stream (False).  Process-wide."""
+    _lib.check("pkv_set_overlap", _lib.load().pkv_set_overlap(1 if on else 0))
+
+
 DECODE_KERNELS = {"auto": 0, "simt": 1, "tensor": 2}
 
 

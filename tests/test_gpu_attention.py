@@ -302,3 +302,34 @@ def test_long_contexts_and_largest_group(prefill_kernel, bs):
     ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
     got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
     assert_close(got, ref, f"long contexts, block size {bs}, prefill={prefill_kernel}")
+
+
+@pytest.fixture
+def overlap_setting():
+    yield
+    ops.set_overlap(True)
+
+
+@pytest.mark.parametrize("case", ["mixed", "random"])
+def test_prefill_beside_decode_matches_serial_order(case, overlap_setting):
+    # the prefill tiles on their own share of the SMs (second stream) or before the decode on
+    # all of them: the same per-item arithmetic, so the prefill rows agree bit for bit; the
+    # decode rows are cut at other split points, so both are held to the oracle
+    if case == "mixed":
+        bt, q_rot, kc, vc, ref = config_with_oracle(5)
+    else:
+        bt = W.make_batch([40, 700, 1, 300, 2048, 64, 900], [40, 200, 1, 1, 130, 1, 1], 16, 8, 128, 400, seed=11)
+        q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                         bt.v_cache, bt.rope_theta)
+        ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc,
+                                     bt.scale)
+    outs = {}
+    for on in (True, False):
+        ops.set_overlap(on)
+        got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+        assert_close(got, ref, f"{bt.name}, prefill beside decode {on}")
+        outs[on] = got
+    qsl = bt.query_start_loc
+    rows = np.concatenate([np.arange(qsl[b], qsl[b + 1]) for b in range(bt.num_seqs) if qsl[b + 1] - qsl[b] > 1])
+    assert len(rows) > 0
+    assert np.array_equal(outs[True][rows], outs[False][rows])

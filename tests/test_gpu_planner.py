@@ -62,3 +62,37 @@ def test_planner_counts_match_oracle_classification(index, prefill):
     # tcgen05 tiles stack the G q heads of a kv head: floor(128 / G) positions per tile
     tile_q = 128 // (bt.num_q_heads // bt.num_kv_heads) if prefill == "tcgen05" else 64
     assert header == _expected(bt, ctas, tile_q)
+
+
+@pytest.mark.parametrize("index", [5])
+def test_split_gives_the_prefill_a_share_and_spreads_decode_units_over_the_rest(index):
+    # header[5] = prefill CTAs that take items.  Beside the decode (default) the planner gives
+    # the prefill P of the SMs and spreads the decode units over the other C - P; in the
+    # serial order every launched prefill CTA takes items and the decode uses all C.
+    bt = W.config(index, poison=False)
+    d = Dev(bt)
+    T, hq, hd = bt.q.shape
+    hkv = bt.num_kv_heads
+    mb = bt.block_tables.shape[1]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tile_q = 128 // (hq // hkv)
+    pf_grid = min((T // tile_q + bt.num_seqs + 1) * hkv, sms)
+    ws = ops.alloc_workspace(T, bt.num_seqs, hq, hkv, hd, mb, device=d.q.device)
+    try:
+        for on in (True, False):
+            ops.set_overlap(on)
+            ws.fill_(0xFF)
+            ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                                workspace=ws)
+            torch.cuda.synchronize()
+            assert ops.get_device_error() == 0
+            h = ws[:24].cpu().numpy().view(np.int32)[:6].tolist()
+            pn = h[5]
+            if on:
+                assert 1 <= pn < sms and pn <= h[3] * hkv
+                assert h[:5] == _expected(bt, sms - pn, tile_q)
+            else:
+                assert pn == pf_grid
+                assert h[:5] == _expected(bt, sms, tile_q)
+    finally:
+        ops.set_overlap(True)
