@@ -144,9 +144,10 @@ int device_sm_count();
 constexpr float kSplitHbmBytesPerNs = 6500.f;
 constexpr float kSplitDecodeSmBytesPerNs = 58.f;
 // One TMA box of the prefill is block_size rows x 128 bytes of one kv head; small boxes
-// arrive more slowly (GB300, boxes from L2: 37 GB/s per SM at 2 KB, 65 GB/s at 16 KB).
+// arrive more slowly (GB300, boxes from L2 alone: 37 GB/s per SM at 2 KB, 65 GB/s at 16 KB;
+// the 16-token prefill tiles beside the decode took in 33.5 GB/s per SM).
 inline float split_prefill_sm_bytes_per_ns(int bs_log2) {
-  return bs_log2 <= 3 ? 26.f : bs_log2 == 4 ? 36.f : bs_log2 == 5 ? 48.f : 58.f;
+  return bs_log2 <= 3 ? 24.f : bs_log2 == 4 ? 34.f : bs_log2 == 5 ? 45.f : 55.f;
 }
 
 struct SplitArgs {

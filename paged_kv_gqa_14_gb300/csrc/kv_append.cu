@@ -3,7 +3,8 @@
 // "Week 4 -- Paged KV cache": pool of fixed-size blocks addressed by slot; the block size is
 // 16 by default and any power of two from 8 to 128 here).
 //
-// One CTA per new token.  The token's d/2 rotation angles are computed once into shared
+// One CTA per new token.  Its q, k and v rows are read first (their addresses do not
+// depend on the position), then the d/2 rotation angles are computed once into shared
 // memory: angle = pos * f_i with f_i = theta^(-2i/d) (fp64 on the host), reduced to
 // [-pi, pi] in fp64, then sincosf in fp32.  Every head of q (in place) and k (into the
 // slot) is rotated pairwise (i, i + d/2) in fp32 and rounded to bf16 nearest-even; v is a
@@ -104,6 +105,10 @@ __device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t n
   slot = (static_cast<int64_t>(blk) << src.bs_log2) + (pos & ((int64_t(1) << src.bs_log2) - 1));
 }
 
+// Row items a thread holds in registers from the start (item = one 16-byte chunk pair of a q
+// or k head, or one 16-byte chunk of a v head; items past these counts are read later).
+constexpr int kQPrefetch = 2;  // covers Hq * d / 16 <= 256 (32 q heads of 128 dims, 64 of 64)
+
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
     bf16* __restrict__ q, int64_t q_st, int64_t q_sh, const bf16* __restrict__ k, int64_t k_st,
@@ -112,21 +117,54 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
     const __grid_constant__ RopeFreqs fr, unsigned int* err) {
   constexpr int HALF = D / 2;
   constexpr int CH = HALF / 8;  // 16-byte chunks per half head
+  constexpr int VCH = D / 8;    // 16-byte chunks per v head
   __shared__ float2 cs[HALF];
   __shared__ int64_t s_pos, s_slot;
 
   pdl_wait();  // q, k, v and the index inputs may come from the previous kernel
   pdl_trigger();
   const int64_t t = blockIdx.x;
-  if (threadIdx.x < 32) {
+  const int tid = threadIdx.x;
+  const int nq = hq * CH, nk = hkv * CH, nv = hkv * VCH;
+  auto q_row = [&](int item, int& c) -> bf16* {
+    const int head = item / CH;
+    c = item - head * CH;
+    return q + t * q_st + head * q_sh;
+  };
+  // The token's rows do not depend on its position or slot: they are read first, so their
+  // latency overlaps the index reads and the angle computation.
+  uint4 qlo[kQPrefetch], qhi[kQPrefetch];
+#pragma unroll
+  for (int j = 0; j < kQPrefetch; ++j) {
+    const int item = tid + j * kAppendThreads;
+    if (item < nq) {
+      int c;
+      const bf16* row = q_row(item, c);
+      qlo[j] = *reinterpret_cast<const uint4*>(row + c * 8);
+      qhi[j] = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
+    }
+  }
+  uint4 klo = make_uint4(0u, 0u, 0u, 0u), khi = klo, vx = klo;
+  if (tid < nk) {
+    const int h = tid / CH, c = tid - (tid / CH) * CH;
+    const bf16* row = k + t * k_st + h * k_sh;
+    klo = *reinterpret_cast<const uint4*>(row + c * 8);
+    khi = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
+  }
+  if (tid < nv) {
+    const int h = tid / VCH, c = tid - (tid / VCH) * VCH;
+    vx = *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8);
+  }
+
+  if (tid < 32) {
     int64_t p_, s_;
     if (src.qsl) {
-      derive_slot(src, t, threadIdx.x, num_slots >> src.bs_log2, err, p_, s_);
+      derive_slot(src, t, tid, num_slots >> src.bs_log2, err, p_, s_);
     } else {
       p_ = src.positions[t];
       s_ = src.slots[t];
     }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       s_pos = p_;
       s_slot = s_;
       if (src.pos_out) src.pos_out[t] = p_;
@@ -137,51 +175,59 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
   const int64_t pos = s_pos;
   const int64_t slot = s_slot;
 
-  for (int i = threadIdx.x; i < HALF; i += kAppendThreads) {
+  for (int i = tid; i < HALF; i += kAppendThreads) {
     const double a = static_cast<double>(pos) * fr.f[i];
     const double n = rint(a * kInvTwoPi);
     const float r = static_cast<float>(fma(-n, kTwoPi, a));
-    float s, c;
-    sincosf(r, &s, &c);
-    cs[i] = make_float2(c, s);
+    float sn, cn;
+    sincosf(r, &sn, &cn);
+    cs[i] = make_float2(cn, sn);
   }
   const bool in_range = slot < num_slots;
   const bool write_kv = slot >= 0 && in_range;
-  if (!in_range && threadIdx.x == 0) raise_error(err, PKV_DEVERR_SLOT_RANGE);
+  if (!in_range && tid == 0) raise_error(err, PKV_DEVERR_SLOT_RANGE);
   __syncthreads();
 
-  // rotations: q heads in place, k heads into the cache row of `slot`
-  const int n_rot = (hq + (write_kv ? hkv : 0)) * CH;
-  for (int item = threadIdx.x; item < n_rot; item += kAppendThreads) {
-    const int head = item / CH;
-    const int c = item - head * CH;
-    const bf16* src;
-    bf16* dst;
-    if (head < hq) {
-      bf16* row = q + t * q_st + head * q_sh;
-      src = row;
-      dst = row;
-    } else {
-      const int h = head - hq;
-      src = k + t * k_st + h * k_sh;
-      dst = k_cache + (slot * hkv + h) * D;
+  // q heads rotated in place
+#pragma unroll
+  for (int j = 0; j < kQPrefetch; ++j) {
+    const int item = tid + j * kAppendThreads;
+    if (item < nq) {
+      int c;
+      bf16* row = q_row(item, c);
+      rotate8(qlo[j], qhi[j], cs + c * 8);
+      *reinterpret_cast<uint4*>(row + c * 8) = qlo[j];
+      *reinterpret_cast<uint4*>(row + HALF + c * 8) = qhi[j];
     }
-    uint4 lo = *reinterpret_cast<const uint4*>(src + c * 8);
-    uint4 hi = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
+  }
+  for (int item = tid + kQPrefetch * kAppendThreads; item < nq; item += kAppendThreads) {
+    int c;
+    bf16* row = q_row(item, c);
+    uint4 lo = *reinterpret_cast<const uint4*>(row + c * 8);
+    uint4 hi = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
     rotate8(lo, hi, cs + c * 8);
+    *reinterpret_cast<uint4*>(row + c * 8) = lo;
+    *reinterpret_cast<uint4*>(row + HALF + c * 8) = hi;
+  }
+  if (!write_kv) return;
+  // k heads rotated into the cache row of `slot`, v heads copied there
+  for (int item = tid; item < nk; item += kAppendThreads) {
+    const int h = item / CH, c = item - (item / CH) * CH;
+    uint4 lo = klo, hi = khi;
+    if (item >= kAppendThreads) {
+      const bf16* row = k + t * k_st + h * k_sh;
+      lo = *reinterpret_cast<const uint4*>(row + c * 8);
+      hi = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
+    }
+    rotate8(lo, hi, cs + c * 8);
+    bf16* dst = k_cache + (slot * hkv + h) * D;
     *reinterpret_cast<uint4*>(dst + c * 8) = lo;
     *reinterpret_cast<uint4*>(dst + HALF + c * 8) = hi;
   }
-
-  // v: plain 16-byte copies
-  if (write_kv) {
-    constexpr int VCH = D / 8;
-    for (int item = threadIdx.x; item < hkv * VCH; item += kAppendThreads) {
-      const int h = item / VCH;
-      const int c = item - h * VCH;
-      const uint4 x = *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8);
-      *reinterpret_cast<uint4*>(v_cache + (slot * hkv + h) * D + c * 8) = x;
-    }
+  for (int item = tid; item < nv; item += kAppendThreads) {
+    const int h = item / VCH, c = item - (item / VCH) * VCH;
+    const uint4 x = item >= kAppendThreads ? *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8) : vx;
+    *reinterpret_cast<uint4*>(v_cache + (slot * hkv + h) * D + c * 8) = x;
   }
 }
 
