@@ -5,10 +5,11 @@
 //
 // One CTA per new token.  Its q, k and v rows are read first (their addresses do not
 // depend on the position), then the d/2 rotation angles are computed once into shared
-// memory: angle = pos * f_i with f_i = theta^(-2i/d) (fp64 on the host), reduced to
-// [-pi, pi] in fp64, then sincosf in fp32.  Every head of q (in place) and k (into the
-// slot) is rotated pairwise (i, i + d/2) in fp32 and rounded to bf16 nearest-even; v is a
-// 16-byte vector copy.  All global accesses are 16-byte vectors along head_dim.
+// memory: angle = pos * f_i with f_i = theta^(-2i/d) (fp64 on the host), taken modulo one
+// turn exactly in 64-bit integer arithmetic (RopeFreqs), then sincosf in fp32.  Every head
+// of q (in place) and k (into the slot) is rotated pairwise (i, i + d/2) in fp32 and rounded
+// to bf16 nearest-even; v is a 16-byte vector copy.  All global accesses are 16-byte
+// vectors along head_dim.
 #include <math.h>
 
 #include "common.cuh"
@@ -33,13 +34,17 @@ struct AppendSrc {
   int64_t* slot_out;
 };
 
+// The rotation frequencies as fractions of a turn in 0.64 fixed point:
+// F_i = round(f_i / (2 pi) * 2^64), f_i = theta^(-2i/d).  The angle of position p is then
+// p f_i = 2 pi (p F_i / 2^64), and its part modulo one turn is the low 64 bits of the integer
+// product p F_i: exact up to the rounding of F_i (at most p / 2^64 of a turn), with no
+// floating-point range reduction.
 struct RopeFreqs {
-  double f[kMaxHeadDim / 2];  // f_i = theta^(-2 i / d), i < d/2
+  unsigned long long F[kMaxHeadDim / 2];
 };
 
-// 2*pi and 1/(2*pi) rounded to double.
-constexpr double kTwoPi = 6.283185307179586476925286766559;
-constexpr double kInvTwoPi = 0.159154943091895335768883763372514;
+// 2 pi / 2^32: radians per unit of the top 32 bits of a 0.64 fixed-point turn.
+constexpr float kTwoPiOver2p32 = 1.4629180792671596e-09f;
 
 __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float2* cs) {
   uint32_t* a = reinterpret_cast<uint32_t*>(&lo);
@@ -176,9 +181,9 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
   const int64_t slot = s_slot;
 
   for (int i = tid; i < HALF; i += kAppendThreads) {
-    const double a = static_cast<double>(pos) * fr.f[i];
-    const double n = rint(a * kInvTwoPi);
-    const float r = static_cast<float>(fma(-n, kTwoPi, a));
+    // the token's angle modulo one turn, as a signed fraction of a turn: r in [-pi, pi)
+    const unsigned long long turn = static_cast<unsigned long long>(pos) * fr.F[i];
+    const float r = static_cast<float>(static_cast<int>(turn >> 32)) * kTwoPiOver2p32;
     float sn, cn;
     sincosf(r, &sn, &cn);
     cs[i] = make_float2(cn, sn);
@@ -233,12 +238,40 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
 
 }  // namespace
 
+namespace {
+
+// round(f / (2 pi) * 2^64) for 0 <= f <= 1, with 2^64 / (2 pi) as a double-double
+// (hi + lo) and the product's rounding error recovered by an FMA, so F is within one unit.
+unsigned long long turn_fraction_0p64(double f) {
+  constexpr double kHi = 2.9358905032820014e+18;  // 2^64 / (2 pi) = kHi + kLo
+  constexpr double kLo = -181.50375616818445;
+  const double p = f * kHi;
+  const double e = fma(f, kHi, -p) + f * kLo;  // f (kHi + kLo) - p
+  const double whole = floor(p);
+  return static_cast<unsigned long long>(static_cast<long long>(whole)) +
+         static_cast<unsigned long long>(llround((p - whole) + e));
+}
+
+// The frequency table of the last (theta, head_dim) seen by this host thread.
+const RopeFreqs& rope_freqs(double theta, int head_dim) {
+  thread_local RopeFreqs table;
+  thread_local double t_theta = -1.0;
+  thread_local int t_dim = -1;
+  if (theta != t_theta || head_dim != t_dim) {
+    const int half = head_dim / 2;
+    for (int i = 0; i < kMaxHeadDim / 2; ++i)
+      table.F[i] = i < half ? turn_fraction_0p64(pow(theta, -2.0 * i / head_dim)) : 0ull;
+    t_theta = theta;
+    t_dim = head_dim;
+  }
+  return table;
+}
+
+}  // namespace
+
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
-  RopeFreqs fr;
-  const int half = a.head_dim / 2;
-  for (int i = 0; i < half; ++i) fr.f[i] = pow(a.theta, -2.0 * i / a.head_dim);
-  for (int i = half; i < kMaxHeadDim / 2; ++i) fr.f[i] = 0.0;
+  const RopeFreqs& fr = rope_freqs(a.theta, a.head_dim);
   const dim3 grid(static_cast<unsigned>(a.num_tokens));
   AppendSrc src;
   src.positions = a.positions;

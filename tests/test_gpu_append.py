@@ -51,6 +51,16 @@ def test_append_matches_oracle_on_workloads(index):
     assert frac_off < 0.01  # 1-ulp differences are rare rounding ties, not a pattern
 
 
+@pytest.mark.parametrize("d,theta", [(128, 1.0e6), (64, 1.0e4)])
+def test_append_large_positions(d, theta):
+    # positions up to 2^24: the kernel takes each angle modulo one turn in 64-bit fixed point;
+    # the oracle's fp64 angle is exact to 2^-28 rad there, well inside the rotation tolerance
+    bt = W.make_batch([3] * 16, [1] * 16, 16, 8 if d == 128 else 4, d, 20, seed=21, rope_theta=theta)
+    bt.positions = np.array([0, 1, 2, 31, 999, 1000, 65535, 65536, 123457, 1_000_003, 4_000_037,
+                             2**22 + 3, 7_777_777, 2**23 - 1, 2**24 - 5, 2**24], dtype=np.int64)
+    _check_append(bt, Dev(bt))
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_append_random_shapes(seed):
     bt = W.random_case(seed, head_dims=(64, 128), groups=(1, 2, 3, 7), kv_heads=(1, 2, 4, 8))
