@@ -221,6 +221,15 @@ def decode_traffic(bt_name):
     return rec["bytes"] if h.hexdigest() == rec["sha"] else None
 
 
+def percentiles(xs):
+    """[p10, p50, p90] of a list of per-launch times (nearest rank), rounded."""
+    v = sorted(xs)
+    if not v:
+        return None
+    pick = lambda q: v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))]  # noqa: E731
+    return [round(pick(0.1), 5), round(pick(0.5), 5), round(pick(0.9), 5)]
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def run_gpu(args, rank, world, local_rank):
     import torch
@@ -438,6 +447,12 @@ def run_gpu(args, rank, world, local_rank):
             "paged_attention_call": round(sum(att_ms) / K, 5),
             "decode_splitk": round(dec_avg, 5),
             "prefill_tiles": round(sum(pre_ms) / K, 5),
+        },
+        "kernels_ms_p10_p50_p90": {
+            "kv_append": percentiles(app_ms),
+            "paged_attention_call": percentiles(att_ms),
+            "decode_splitk": percentiles(dec_ms),
+            "prefill_tiles": percentiles(pre_ms),
         },
         "roofline": {
             "kernel": "decode_splitk",
