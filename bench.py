@@ -385,23 +385,63 @@ def run_gpu(args, rank, world, local_rank):
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = stg.nbytes
     d2h = host_out.numel() * host_out.element_size()
+    # The result of step i goes back on a second stream while step i + 1 uploads and runs:
+    # `out` is double-buffered, and step i + 2 writes its buffer only after that buffer's
+    # copy back has finished (the two copies use the two directions of the host link).  In
+    # flush mode every step is timed alone, nothing overlaps, and the copy back stays on the
+    # step's own stream.
+    d2h_stream = stream if flush else torch.cuda.Stream(device=dev)
+    outs = [out, torch.empty_like(out)]
+    out_ready = [torch.cuda.Event(), torch.cuda.Event()]  # attention wrote outs[j]
+    out_free = [torch.cuda.Event(), torch.cuda.Event()]   # outs[j] is back on the host
+    for j in range(2):
+        out_free[j].record(stream)
+    e2e_no = [0]
 
     def e2e_step():
+        if flush:  # one step alone: upload, step, copy back, all on the step's stream
+            stg.upload(stream)
+            ops.kv_append(sd.q, sd.k, sd.v, sd.positions, sd.slot_mapping, kc, vc, bt.rope_theta)
+            ops.paged_attention(sd.q, kc, vc, sd.block_tables, sd.context_lens, sd.query_start_loc, bt.scale,
+                                out=out, workspace=ws)
+            if kernel_copy:
+                ops.copy(host_out, out)
+            else:
+                host_out.copy_(out, non_blocking=True)
+            return
+        j = e2e_no[0] & 1
+        e2e_no[0] += 1
         stg.upload(stream)
         ops.kv_append(sd.q, sd.k, sd.v, sd.positions, sd.slot_mapping, kc, vc, bt.rope_theta)
-        ops.paged_attention(sd.q, kc, vc, sd.block_tables, sd.context_lens, sd.query_start_loc, bt.scale, out=out,
-                            workspace=ws)
+        stream.wait_event(out_free[j])
+        ops.paged_attention(sd.q, kc, vc, sd.block_tables, sd.context_lens, sd.query_start_loc, bt.scale,
+                            out=outs[j], workspace=ws)
+        out_ready[j].record(stream)
+        d2h_stream.wait_event(out_ready[j])
         if kernel_copy:
-            ops.copy(host_out, out)
+            ops.copy(host_out, outs[j], stream=d2h_stream)
         else:
-            host_out.copy_(out, non_blocking=True)
+            with torch.cuda.stream(d2h_stream):
+                host_out.copy_(outs[j], non_blocking=True)
+        out_free[j].record(d2h_stream)
+
+    def e2e_steps_joined(n):
+        """n end-to-end steps; the timed region ends when the last result is on the host."""
+        def run():
+            for _ in range(n):
+                e2e_step()
+            if d2h_stream is not stream:
+                stream.wait_stream(d2h_stream)
+        return run
 
     for _ in range(args.warmup):
         e2e_step()
+    if d2h_stream is not stream:
+        stream.wait_stream(d2h_stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    e2e_ms = timed(e2e_step, K)
+    e2e_ms = timed(e2e_steps_joined(K), 1) / K if not flush else timed(e2e_steps_joined(1), K)
     e2e_ms = replicas.max_over_ranks(e2e_ms, dist, device=dev)
     assert ops.get_device_error() == 0, "device error during timing"
 
@@ -477,6 +517,9 @@ def run_gpu(args, rank, world, local_rank):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "copy": args.e2e_copy,
+            "pipeline": ("each step alone: upload, step, result copied back, on one stream" if flush else
+                         "each step's result copied back on a second stream while the next step uploads and "
+                         "runs (double-buffered out); the timed region ends with the last result on the host"),
         },
         "gpu_launches": 4 * K,  # kv_append, planner, prefill tiles, decode split-K (+ merge)
         "clocks": clk,

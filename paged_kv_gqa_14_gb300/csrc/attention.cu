@@ -13,6 +13,7 @@
 // the prefill kernel on a second stream, forked after the planner and joined back before
 // the call returns, at the same time as the decode: the planner gives the prefill P of
 // the SMs and spreads the decode units over the rest (SplitArgs in internal.h).
+#include <cstring>
 #include <mutex>
 
 #include "decode.cuh"
@@ -41,22 +42,65 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
+// Encodes a bf16, 128-byte-swizzled tiled tensor map, reusing the last few encodings made
+// on this host thread: a serving loop passes the same pool (and often the same q buffer)
+// every step, and the key holds every input of the encoding, so a hit is the same map.
+bool encode_bf16_sw128(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box) {
+  struct Key {
+    const void* base;
+    int rank;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5];
+  };
+  struct Entry {
+    Key key;
+    CUtensorMap map;
+    bool valid;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  if (rank < 1 || rank > 5) return false;
+  Key key;
+  memset(&key, 0, sizeof(key));
+  key.base = base;
+  key.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides[i];
+  }
+  for (Entry& e : cache)
+    if (e.valid && memcmp(&e.key, &key, sizeof(Key)) == 0) {
+      *m = e.map;
+      return true;
+    }
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims,
+         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache[next].key = key;
+  cache[next].map = *m;
+  cache[next].valid = true;
+  next = (next + 1) % kEntries;
+  return true;
+}
+
 // The pool [num_blocks][block_size][Hkv][d] as a 4-D tensor {d, Hkv, block_size, num_blocks};
 // a box is all block_size token rows x 64 dims of one kv head in one block, 128-byte swizzled
 // (the tcgen05 prefill's K/V tiles).
 bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
   const cuuint64_t bs = cuuint64_t(1) << bs_log2;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv), bs,
                               static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hkv) * D * 2,
                                  bs * hkv * D * 2};
   const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(bs), 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16_sw128(m, base, 4, dims, strides, box);
 }
 
 namespace {
@@ -327,18 +371,13 @@ cudaError_t launch_decode_g(const AttnArgs& a, cudaStream_t stream) {
 
 // q [T][Hq][d] as a 3-D tensor {d, Hq, T}; a box is 128 token rows x 64 dims of one head.
 bool make_q_map(CUtensorMap* m, const AttnArgs& a) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.head_dim), static_cast<cuuint64_t>(a.hq),
                               static_cast<cuuint64_t>(a.num_tokens)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.q_sh) * 2, static_cast<cuuint64_t>(a.q_st) * 2};
   // a box is the G heads of one kv head's group x P consecutive tokens x 64 dims
   const int g = a.hq / a.hkv;
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(kTcPrefillRows / g)};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16_sw128(m, a.q, 3, dims, strides, box);
 }
 
 bool make_prefill_tc_params(const AttnArgs& a, PrefillTcParams* P) {
@@ -385,18 +424,13 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaS
 // (a row, a head, a block); a box is 64 dims x min(block_size, 16) rows x all kv heads of one
 // block, 128-byte swizzled, landing as [kv head][rows][128 bytes].
 bool make_pool_map_heads(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
   const cuuint64_t bs = cuuint64_t(1) << bs_log2;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), bs, static_cast<cuuint64_t>(hkv),
                               static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(hkv) * D * 2, static_cast<cuuint64_t>(D) * 2,
                                  bs * hkv * D * 2};
   const cuuint32_t box[4] = {64, bs < 16 ? static_cast<cuuint32_t>(bs) : 16u, static_cast<cuuint32_t>(hkv), 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16_sw128(m, base, 4, dims, strides, box);
 }
 
 cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {

@@ -18,7 +18,15 @@ BLOCK_SIZE = 16  # the pool's default block size
 SUPPORTED_BLOCK_SIZES = (8, 16, 32, 64, 128)
 
 
+# The current stream's raw handle without building a torch.cuda.Stream object (about 0.1 us
+# instead of 3 us per call on the Grace host); torch.cuda.current_stream() where torch lacks it.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream_ptr(stream):
+    if stream is None and _raw_stream is not None and _cur_device is not None:
+        return ctypes.c_void_p(_raw_stream(_cur_device()))
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
 

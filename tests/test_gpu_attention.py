@@ -310,7 +310,7 @@ def overlap_setting():
     ops.set_overlap(True)
 
 
-@pytest.mark.parametrize("case", ["mixed", "random"])
+@pytest.mark.parametrize("case", ["mixed", "random", "prefill-heavy", "prefill-only"])
 def test_prefill_beside_decode_matches_serial_order(case, overlap_setting):
     # the prefill tiles on their own share of the SMs (second stream) or before the decode on
     # all of them: the same per-item arithmetic, so the prefill rows agree bit for bit; the
@@ -318,7 +318,14 @@ def test_prefill_beside_decode_matches_serial_order(case, overlap_setting):
     if case == "mixed":
         bt, q_rot, kc, vc, ref = config_with_oracle(5)
     else:
-        bt = W.make_batch([40, 700, 1, 300, 2048, 64, 900], [40, 200, 1, 1, 130, 1, 1], 16, 8, 128, 400, seed=11)
+        if case == "random":
+            ctx, spans = [40, 700, 1, 300, 2048, 64, 900], [40, 200, 1, 1, 130, 1, 1]
+        elif case == "prefill-heavy":  # most SMs go to the prefill; three decodes
+            ctx, spans = [3000, 2500, 4096, 700, 33, 1500], [512, 1000, 700, 1, 1, 1]
+        else:  # no decode units at all
+            ctx, spans = [800, 1200, 65], [800, 300, 65]
+        pages = sum(-(-c // 16) for c in ctx)
+        bt = W.make_batch(ctx, spans, 16, 8, 128, pages + 8, seed=11)
         q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
                                          bt.v_cache, bt.rope_theta)
         ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc,

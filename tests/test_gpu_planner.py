@@ -64,12 +64,16 @@ def test_planner_counts_match_oracle_classification(index, prefill):
     assert header == _expected(bt, ctas, tile_q)
 
 
-@pytest.mark.parametrize("index", [5])
-def test_split_gives_the_prefill_a_share_and_spreads_decode_units_over_the_rest(index):
+@pytest.mark.parametrize("case", ["mixed", "prefill-heavy"])
+def test_split_gives_the_prefill_a_share_and_spreads_decode_units_over_the_rest(case):
     # header[5] = prefill CTAs that take items.  Beside the decode (default) the planner gives
     # the prefill P of the SMs and spreads the decode units over the other C - P; in the
     # serial order every launched prefill CTA takes items and the decode uses all C.
-    bt = W.config(index, poison=False)
+    if case == "mixed":
+        bt = W.config(5, poison=False)
+    else:  # three long chunks and three short decodes: most SMs belong to the prefill
+        ctx, spans = [3000, 2500, 4096, 700, 33, 1500], [512, 1000, 700, 1, 1, 1]
+        bt = W.make_batch(ctx, spans, 16, 8, 128, sum(-(-c // 16) for c in ctx) + 8, seed=11, poison=False)
     d = Dev(bt)
     T, hq, hd = bt.q.shape
     hkv = bt.num_kv_heads
@@ -91,6 +95,8 @@ def test_split_gives_the_prefill_a_share_and_spreads_decode_units_over_the_rest(
             if on:
                 assert 1 <= pn < sms and pn <= h[3] * hkv
                 assert h[:5] == _expected(bt, sms - pn, tile_q)
+                if case == "prefill-heavy":
+                    assert pn >= sms // 2
             else:
                 assert pn == pf_grid
                 assert h[:5] == _expected(bt, sms, tile_q)
