@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(128) prefill_kernel(const __grid_constant__ Pr
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, tig = lane & 3;
-  pdl_wait();  // the tile list is written by the planner kernel
+  pdl_wait();  // the tile list is written by the planner kernel (on a second stream an event orders it)
   pdl_trigger();
   const int n_tiles = p.plan.header[3];
   const int total = n_tiles * p.hq;

@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   __syncthreads();
   tc5::fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // the tile list is written by the planner kernel
+  pdl_wait();  // the tile list is written by the planner kernel (on a second stream an event orders it)
   pdl_trigger();
   const int n_tiles = p.plan.header[3];
   const int total = n_tiles * p.hkv;
