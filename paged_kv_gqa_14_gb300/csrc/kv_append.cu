@@ -18,7 +18,12 @@
 namespace pkv {
 namespace {
 
-constexpr int kAppendThreads = 128;
+// Threads per token: four warps, or two when the step has more tokens than one wave of
+// four-warp CTAs holds (8 CTAs of 128 threads per SM at 64 registers): 16 two-warp CTAs fit on
+// an SM, so the mixed chunked-prefill step's 2248 tokens run in one wave on 152 SMs.  Measured
+// on GB300: two warps take the 2248-token append from 12.6 to 11.6 us but make the 256-token
+// decode step 2 us slower (eager), so the choice follows the token count.
+constexpr int kAppendWaveCtas = 8;  // four-warp CTAs resident per SM
 
 // Where each token's position and slot come from: explicit arrays, or (qsl != nullptr)
 // derived on the device from the scheduler's tables.
@@ -112,10 +117,10 @@ __device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t n
 
 // Row items a thread holds in registers from the start (item = one 16-byte chunk pair of a q
 // or k head, or one 16-byte chunk of a v head; items past these counts are read later).
-constexpr int kQPrefetch = 2;  // covers Hq * d / 16 <= 256 (32 q heads of 128 dims, 64 of 64)
+constexpr int kQPrefetch = 2;  // q chunk pairs per thread: Hq * d / 16 <= 2 x threads
 
-template <int D>
-__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
+template <int D, int kAppendThreads>
+__global__ void __launch_bounds__(kAppendThreads, kAppendThreads == 64 ? 16 : kAppendWaveCtas) kv_append_kernel(
     bf16* __restrict__ q, int64_t q_st, int64_t q_sh, const bf16* __restrict__ k, int64_t k_st,
     int64_t k_sh, const bf16* __restrict__ v, int64_t v_st, int64_t v_sh, const __grid_constant__ AppendSrc src,
     bf16* __restrict__ k_cache, bf16* __restrict__ v_cache, int64_t num_slots, int hq, int hkv,
@@ -123,6 +128,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
   constexpr int HALF = D / 2;
   constexpr int CH = HALF / 8;  // 16-byte chunks per half head
   constexpr int VCH = D / 8;    // 16-byte chunks per v head
+  constexpr int kVPrefetch = 128 / kAppendThreads;  // v chunks per thread: Hkv * d / 8 <= 128
   __shared__ float2 cs[HALF];
   __shared__ int64_t s_pos, s_slot;
 
@@ -149,16 +155,21 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
       qhi[j] = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
     }
   }
-  uint4 klo = make_uint4(0u, 0u, 0u, 0u), khi = klo, vx = klo;
+  uint4 klo = make_uint4(0u, 0u, 0u, 0u), khi = klo, vx[kVPrefetch];
   if (tid < nk) {
     const int h = tid / CH, c = tid - (tid / CH) * CH;
     const bf16* row = k + t * k_st + h * k_sh;
     klo = *reinterpret_cast<const uint4*>(row + c * 8);
     khi = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
   }
-  if (tid < nv) {
-    const int h = tid / VCH, c = tid - (tid / VCH) * VCH;
-    vx = *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8);
+#pragma unroll
+  for (int j = 0; j < kVPrefetch; ++j) {
+    const int item = tid + j * kAppendThreads;
+    vx[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (item < nv) {
+      const int h = item / VCH, c = item - (item / VCH) * VCH;
+      vx[j] = *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8);
+    }
   }
 
   if (tid < 32) {
@@ -229,10 +240,18 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
     *reinterpret_cast<uint4*>(dst + c * 8) = lo;
     *reinterpret_cast<uint4*>(dst + HALF + c * 8) = hi;
   }
-  for (int item = tid; item < nv; item += kAppendThreads) {
+#pragma unroll
+  for (int j = 0; j < kVPrefetch; ++j) {
+    const int item = tid + j * kAppendThreads;
+    if (item < nv) {
+      const int h = item / VCH, c = item - (item / VCH) * VCH;
+      *reinterpret_cast<uint4*>(v_cache + (slot * hkv + h) * D + c * 8) = vx[j];
+    }
+  }
+  for (int item = tid + kVPrefetch * kAppendThreads; item < nv; item += kAppendThreads) {
     const int h = item / VCH, c = item - (item / VCH) * VCH;
-    const uint4 x = item >= kAppendThreads ? *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8) : vx;
-    *reinterpret_cast<uint4*>(v_cache + (slot * hkv + h) * D + c * 8) = x;
+    *reinterpret_cast<uint4*>(v_cache + (slot * hkv + h) * D + c * 8) =
+        *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8);
   }
 }
 
@@ -273,6 +292,7 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
   const RopeFreqs& fr = rope_freqs(a.theta, a.head_dim);
   const dim3 grid(static_cast<unsigned>(a.num_tokens));
+  const bool two_warps = a.num_tokens > static_cast<int64_t>(kAppendWaveCtas) * device_sm_count();
   AppendSrc src;
   src.positions = a.positions;
   src.slots = a.slots;
@@ -286,8 +306,10 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   src.pos_out = a.positions_out;
   src.slot_out = a.slots_out;
   record_kernel_event(PKV_KERNEL_APPEND, false, stream);
+  auto* kernel = a.head_dim == 128 ? (two_warps ? kv_append_kernel<128, 64> : kv_append_kernel<128, 128>)
+                                   : (two_warps ? kv_append_kernel<64, 64> : kv_append_kernel<64, 128>);
   const cudaError_t e = launch_pdl(
-      a.head_dim == 128 ? kv_append_kernel<128> : kv_append_kernel<64>, grid, dim3(kAppendThreads), 0, stream,
+      kernel, grid, dim3(two_warps ? 64 : 128), 0, stream,
       static_cast<bf16*>(a.q), a.q_st, a.q_sh, static_cast<const bf16*>(a.k), a.k_st, a.k_sh,
       static_cast<const bf16*>(a.v), a.v_st, a.v_sh, src, static_cast<bf16*>(a.k_cache),
       static_cast<bf16*>(a.v_cache), a.num_slots, a.hq, a.hkv, fr, a.err);
