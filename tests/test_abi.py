@@ -119,6 +119,13 @@ def test_set_decode_ctas(lib):
     assert lib.pkv_set_kernel_events(0, None, None) == 0
 
 
+def test_set_overlap(lib):
+    assert lib.pkv_set_overlap(2) == 2
+    assert lib.pkv_set_overlap(-1) == 2
+    assert lib.pkv_set_overlap(0) == 0
+    assert lib.pkv_set_overlap(1) == 0
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,54 @@
+"""bench.py's JSON line on the CPU: the reference arm (the oracle on the host cores) on the
+tiny workload, and the helpers the GPU arm reports with."""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "1",
+                          "--steps", "2", "--warmup", "3", "--cpu-budget", "1"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [x for x in out.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == bench.UNIT
+    assert j["steps"] == 2 and j["warmup"] == 3 and j["higher_is_better"] is True
+    assert j["value"] > 0 and j["ms_per_step"] > 0
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["cpu_baseline"]["value"] == j["value"]
+    assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert j["config"]["workload"] == "tiny-decode"
+
+
+def test_warmup_below_three_is_refused():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert out.returncode != 0 and "--warmup must be >= 3" in out.stderr
+
+
+def test_percentiles_nearest_rank():
+    assert bench.percentiles([5, 1, 2, 3, 4, 6, 7, 8, 9, 10]) == [2, 5, 9]
+    assert bench.percentiles([0.25]) == [0.25, 0.25, 0.25]
+    assert bench.percentiles([]) is None
+
+
+@pytest.mark.parametrize("index", [1, 2])
+def test_small_workloads_are_timed_with_an_l2_flush(index):
+    # the tiny and Qwen2.5-0.5B batches hold far less KV than twice the 129 MB L2, so the GPU
+    # arm flushes L2 (a scratch write of FLUSH_BYTES) before each of their timed steps
+    from paged_kv_gqa_14_gb300 import workloads as W
+
+    bt = W.config(index, poison=False)
+    assert bench.kv_unique_bytes(bt) < 2 * bench.L2_BYTES
+    assert bench.FLUSH_BYTES >= 2 * bench.L2_BYTES
