@@ -117,16 +117,23 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def threads_used(cpu_s, wall_s):
+    """Threads a run kept busy on average: its process CPU time over its wall time."""
+    return max(1, int(round(cpu_s / max(wall_s, 1e-9))))
+
+
 def time_oracle(bt, budget_s=12.0, min_seqs=2):
-    """Time the oracle on the first n sequences, n grown until a step costs ~budget/4."""
+    """Time the oracle on the first n sequences, n grown until a step costs ~budget/4.
+    Returns (sub-batch, wall seconds, n, threads used)."""
     n = min_seqs
     while True:
         sb = sub_batch(bt, range(n))
-        t0 = time.perf_counter()
+        c0, t0 = time.process_time(), time.perf_counter()
         oracle_step(sb)
         dt = time.perf_counter() - t0
+        cpu = time.process_time() - c0
         if dt > budget_s / 4 or n >= bt.num_seqs:
-            return sb, dt, n
+            return sb, dt, n, threads_used(cpu, dt)
         n = min(bt.num_seqs, max(n + 1, int(n * min(8.0, (budget_s / 4) / max(dt, 1e-3)))))
 
 
@@ -526,12 +533,13 @@ def run_gpu(args, rank, world, local_rank):
         "decode_seqs": n_decode,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        sb, dt, n = time_oracle(bt, budget_s=args.cpu_budget)
+        sb, dt, n, used = time_oracle(bt, budget_s=args.cpu_budget)
         kv_s = kv_unique_bytes(sb)
         line["cpu_baseline"] = {
             "value": round(kv_s / dt / 1e9, 4),
             "unit": UNIT,
-            "cores": host_cores(),
+            "cores": used,
+            "cores_available": host_cores(),
             "kind": "oracle",
             "sample": f"first {n} of {bt.num_seqs} sequences of {bt.name} ({kv_s / 1e6:.1f} MB unique KV), "
                       f"oracle kv_append + paged_attention, one pass {dt:.2f} s",
@@ -544,15 +552,17 @@ def run_gpu(args, rank, world, local_rank):
 # ----------------------------------------------------------------------- reference arm
 def run_reference(args):
     bt = W.config(args.workload, poison=False, block_size=args.block_size)
-    sb, dt, n = time_oracle(bt, budget_s=min(args.cpu_budget, 8.0))
+    sb, dt, n, _ = time_oracle(bt, budget_s=min(args.cpu_budget, 8.0))
     kv_s = kv_unique_bytes(sb)
     for _ in range(args.warmup):
         oracle_step(sb)
     times = []
+    c0 = time.process_time()
     for _ in range(args.steps):
         t0 = time.perf_counter()
         oracle_step(sb)
         times.append(time.perf_counter() - t0)
+    used = threads_used(time.process_time() - c0, sum(times))
     ms = 1e3 * sum(times) / len(times)
     value = round(kv_s / (ms * 1e-3) / 1e9, 4)
     return {
@@ -573,7 +583,8 @@ def run_reference(args):
         "cpu_baseline": {
             "value": value,
             "unit": UNIT,
-            "cores": host_cores(),
+            "cores": used,
+            "cores_available": host_cores(),
             "kind": "oracle",
             "sample": f"first {n} of {bt.num_seqs} sequences of {bt.name} per step ({kv_s / 1e6:.1f} MB unique KV)",
         },

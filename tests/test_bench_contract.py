@@ -25,7 +25,8 @@ def test_reference_arm_prints_one_json_line():
     assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == bench.UNIT
     assert j["steps"] == 2 and j["warmup"] == 3 and j["higher_is_better"] is True
     assert j["value"] > 0 and j["ms_per_step"] > 0
-    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["cpu_baseline"]["kind"] == "oracle"
+    assert 1 <= j["cpu_baseline"]["cores"] <= j["cpu_baseline"]["cores_available"]
     assert j["cpu_baseline"]["value"] == j["value"]
     assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert j["config"]["workload"] == "tiny-decode"
@@ -35,6 +36,12 @@ def test_warmup_below_three_is_refused():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "1"],
                          capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0 and "--warmup must be >= 3" in out.stderr
+
+
+def test_threads_used_is_cpu_time_over_wall_time():
+    assert bench.threads_used(16.0, 1.0) == 16
+    assert bench.threads_used(0.4, 1.0) == 1
+    assert bench.threads_used(0.0, 0.0) == 1
 
 
 def test_percentiles_nearest_rank():
