@@ -143,12 +143,11 @@ int device_sm_count();
 // SMs: every CTA computes what it would compute in the serial order.
 constexpr float kSplitHbmBytesPerNs = 6500.f;
 constexpr float kSplitDecodeSmBytesPerNs = 58.f;
-// One TMA box of the prefill is block_size rows x 128 bytes of one kv head; small boxes
-// arrive more slowly (GB300, boxes from L2 alone: 37 GB/s per SM at 2 KB, 65 GB/s at 16 KB;
-// the 16-token prefill tiles beside the decode took in 33.5 GB/s per SM).
-inline float split_prefill_sm_bytes_per_ns(int bs_log2) {
-  return bs_log2 <= 3 ? 24.f : bs_log2 == 4 ? 34.f : bs_log2 == 5 ? 45.f : 55.f;
-}
+// The prefill tiles' pace per SM, measured beside the decode on GB300 (mixed chunked-prefill
+// batch): about 1.95 us per 128-key K/V tile of 64 KB, i.e. 33.5 GB/s per SM, at 16-, 32-, 64-
+// and 128-token blocks alike (the tile's TMA boxes grow with the block, the pace does not),
+// and 29 GB/s at 8-token blocks (two half-height boxes per page).
+inline float split_prefill_sm_bytes_per_ns(int bs_log2) { return bs_log2 <= 3 ? 29.f : 33.5f; }
 
 struct SplitArgs {
   int on;             // 1: the planner splits `sms` CTAs between prefill and decode
