@@ -39,6 +39,7 @@ from paged_kv_gqa_14_gb300 import workloads as W  # noqa: E402
 METRIC = "paged decode attention achieved KV GB/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 10**6     # GB300 L2
 FLUSH_BYTES = 256 << 20    # scratch written between timed steps in flush mode (> 2 x L2)
 
@@ -99,6 +100,19 @@ def sub_batch(bt, seqs):
                    positions=bt.positions[rows], slot_mapping=new_slots, k_cache=bt.k_cache[idx],
                    v_cache=bt.v_cache[idx], block_tables=tables, context_lens=bt.context_lens[seqs],
                    query_start_loc=np.array(qsl, dtype=np.int32), scale=bt.scale, rope_theta=bt.rope_theta)
+
+
+def prefill_flops(bt):
+    """Algorithmic FLOPs of the prefill spans (n > 1 rows): 4 d per unmasked (query, key) pair
+    per q head (QK^T and P.V, two flops per multiply-add).  Row r of an n-row span over ctx keys
+    sees ctx - n + r + 1 keys."""
+    pairs = 0
+    for b in range(bt.num_seqs):
+        n = int(bt.query_start_loc[b + 1] - bt.query_start_loc[b])
+        if n > 1:
+            ctx = int(bt.context_lens[b])
+            pairs += n * (ctx - n + 1) + n * (n - 1) // 2
+    return 4 * bt.head_dim * bt.num_q_heads * pairs
 
 
 def oracle_step(sb):
@@ -187,45 +201,107 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------ peaks
-def hbm_peak():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _peaks():
     try:
-        with open(path) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def hbm_peak():
+    try:
+        return float(_peaks()["hbm_gbs"]), "measured"
+    except (KeyError, TypeError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_traffic(bt_name):
-    """Per-launch DRAM traffic of the decode kernel from the committed ncu summary
-    (profiles/decode_tc_traffic_decode-workloads.md), if it was taken on the current kernel
-    sources and covers this workload; else None."""
+def bf16_peak():
+    """Dense bf16 tensor peak in TFLOP/s: the measured burst figure (a kernel timed on its own
+    inside a short step), else the fallback."""
+    try:
+        return float(_peaks()["bf16_tflops"]), "measured (burst)"
+    except (KeyError, TypeError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ---------------------------------------------------------- DRAM traffic from ncu captures
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kernel_traffic.json")
+KERNEL_PATTERNS = {"decode": "decode_tc_kernel", "prefill": "prefill_tc_kernel"}
+
+
+def source_sha256():
+    """SHA-256 over the library's sources (header and every file of csrc/): a recorded
+    traffic figure stands only for the code it was measured on."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", "decode_tc_traffic_decode-workloads.md")
-    try:
-        with open(path) as f:
-            lines = f.read().splitlines()
-    except OSError:
-        return None
-    rec = {}
-    for line in lines:
-        if line.startswith("source_sha256:"):
-            rec["sha"] = line.split(":", 1)[1].strip()
-        elif line.startswith("sources:"):
-            rec["sources"] = [x.strip() for x in line.split(":", 1)[1].split(",")]
-        elif line.startswith("| ") and line.split("|")[1].strip() == bt_name:
-            rec["bytes"] = float(line.split("|")[7])
-    if "bytes" not in rec or "sha" not in rec:
-        return None
     h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_gqa_14_gb300", "csrc")
+    for path in [os.path.join(ROOT, "include", "pkv.h")] + [os.path.join(csrc, f) for f in sorted(os.listdir(csrc))]:
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def kernel_traffic(kernel, workload):
+    """Recorded DRAM bytes per launch of `kernel` on `workload`, or None when there is no record
+    or it was taken on other sources."""
     try:
-        for name in rec.get("sources", []):
-            with open(os.path.join(ROOT, name), "rb") as f:
-                h.update(f.read())
-    except OSError:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)["records"][f"{kernel}/{workload}"]
+    except (OSError, ValueError, KeyError):
         return None
-    return rec["bytes"] if h.hexdigest() == rec["sha"] else None
+    return float(rec["dram_bytes_per_launch"]) if rec.get("source_sha256") == source_sha256() else None
+
+
+_UNIT = {"byte": 1, "b": 1, "kbyte": 1e3, "kb": 1e3, "mbyte": 1e6, "mb": 1e6, "gbyte": 1e9, "gb": 1e9}
+
+
+def parse_ncu_dram(csv_path, pattern):
+    """Per-launch (read, write) DRAM bytes of the kernels whose name contains `pattern`, from an
+    ``ncu --csv --metrics dram__bytes_read.sum,dram__bytes_write.sum`` log."""
+    import csv
+
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    launches = {}
+    for row in csv.DictReader(lines):
+        if pattern not in row.get("Kernel Name", ""):
+            continue
+        name = row.get("Metric Name", "")
+        if name not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        val = float(row["Metric Value"].replace(",", "")) * _UNIT.get(row.get("Metric Unit", "byte").lower(), 1)
+        launches.setdefault(row["ID"], {})[name] = val
+    return [(v["dram__bytes_read.sum"], v["dram__bytes_write.sum"]) for v in launches.values()
+            if len(v) == 2]
+
+
+def record_traffic(csv_path, kernel, workload, command):
+    """Store the mean DRAM bytes per launch of an ncu capture for (kernel, workload), stamped
+    with the current sources' hash (run right after the capture, on the same sources)."""
+    got = parse_ncu_dram(csv_path, KERNEL_PATTERNS[kernel])
+    if not got:
+        raise SystemExit(f"no {kernel} launches with DRAM metrics in {csv_path}")
+    try:
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    data.setdefault("about", "DRAM traffic per kernel launch (dram__bytes_read.sum + dram__bytes_write.sum) "
+                              "from ncu captures; written by `bench.py --record-traffic`; valid while "
+                              "source_sha256 equals the hash of include/pkv.h and csrc/")
+    rd = sum(r for r, _ in got) / len(got)
+    wr = sum(w for _, w in got) / len(got)
+    data.setdefault("records", {})[f"{kernel}/{workload}"] = {
+        "kernel": KERNEL_PATTERNS[kernel], "workload": workload, "launches": len(got),
+        "dram_read_bytes": round(rd), "dram_write_bytes": round(wr), "dram_bytes_per_launch": round(rd + wr),
+        "source_sha256": source_sha256(), "command": command}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return data["records"][f"{kernel}/{workload}"]
 
 
 def percentiles(xs):
@@ -359,7 +435,33 @@ def run_gpu(args, rank, world, local_rank):
     dec_avg = sum(dec_ms) / K
     peak, peak_kind = hbm_peak()
     achieved = algo / (dec_avg * 1e-3) / 1e9
-    traffic = decode_traffic(bt.name)
+    traffic = kernel_traffic("decode", bt.name)
+    # the prefill tiles' tensor-core roofline (batches with prefill spans): unmasked-pair FLOPs
+    # over the prefill kernel's mean event time, against the bf16 peak; beside the decode also
+    # per SM over the share of the SMs the planner gave it (workspace header word 5)
+    pf_flops = prefill_flops(bt)
+    roofline_prefill = None
+    if pf_flops:
+        pre_avg = sum(pre_ms) / K
+        tpeak, tpeak_kind = bf16_peak()
+        pf_tf = pf_flops / (pre_avg * 1e-3) / 1e12
+        pf_ctas = int(ws[:64].view(torch.int32)[5].item())
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        roofline_prefill = {
+            "kernel": "prefill_tiles",
+            "bound": "tensor",
+            "achieved": round(pf_tf, 1),
+            "peak": tpeak,
+            "peak_source": tpeak_kind,
+            "unit": "TFLOP/s",
+            "frac": round(pf_tf / tpeak, 4),
+            "traffic": kernel_traffic("prefill", bt.name),
+            "algorithmic_flops": pf_flops,
+            "ms": round(pre_avg, 5),
+            "prefill_ctas": pf_ctas,
+            "sms": sms,
+            "frac_of_its_sms": round(pf_tf / (tpeak * max(1, min(pf_ctas, sms)) / sms), 4),
+        }
 
     # the same step captured once in a CUDA graph and replayed (host launch cost removed)
     graph = torch.cuda.CUDAGraph()
@@ -512,6 +614,7 @@ def run_gpu(args, rank, world, local_rank):
             "traffic": traffic,
             "algorithmic_bytes": algo,
         },
+        "roofline_prefill": roofline_prefill,
         "graph": {
             "ms_per_step": round(graph_ms, 5),
             "value": round(world * kv_u / (graph_ms * 1e-3) / 1e9, 2),
@@ -611,10 +714,26 @@ def main():
                     help="prefill tiles before the decode on one stream (default: beside it, SMs split)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="no benchmark: store the DRAM bytes per launch of an ncu capture "
+                         "(--csv --print-units base --metrics dram__bytes_read.sum,dram__bytes_write.sum) of "
+                         "--kernel on --workload in profiles/kernel_traffic.json, stamped with the sources' hash")
+    ap.add_argument("--kernel", choices=sorted(KERNEL_PATTERNS), default="decode")
+    ap.add_argument("--command", default="", help="the capture command, stored with --record-traffic")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.record_traffic:
+        name = W.CONFIG_NAMES[args.workload] + ("" if args.block_size == W.BLOCK_SIZE else f"-bs{args.block_size}")
+        if args.seqs:
+            name += f"-sample{args.seqs}"
+        rec = record_traffic(args.record_traffic, args.kernel, name, args.command)
+        print(json.dumps(rec))
+        return
     rank, world, local_rank = replicas.rank_info()
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but {world} process(es) (WORLD_SIZE): start N > 1 replicas with "
+                 f"`python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus} ...`")
     if args.impl == "reference":
         if rank != 0:
             return

@@ -96,7 +96,11 @@ PKV_API int pkv_version(void);
  *     k_cache[s/bs, s%bs, h, :] <- bf16(rope(k[t, h, :], positions[t]))   for every kv head
  *     v_cache[s/bs, s%bs, h, :] <- v[t, h, :]                              (bit copy)
  *   (bs = block_size)
- * Rotation: fp32 arithmetic on an angle reduced in fp64; rounding to bf16 nearest-even.
+ * Rotation: the angle pos * f_i is reduced modulo one turn exactly in 64-bit fixed point
+ * (pkv_rope_turn_table), then to a quarter turn and an fp32 remainder in [-pi/4, pi/4];
+ * sincosf and the pairwise rotation run in fp32; rounding to bf16 nearest-even.  Before that
+ * rounding a rotated value is within 2.7e-7 (|x_i| + |x_{i+d/2}|) of the exact rotation of
+ * the bf16 inputs (positions below 2^31).
  * A negative slot marks padding and writes nothing.  A slot >= num_blocks*bs is skipped
  * and sets PKV_DEVERR_SLOT_RANGE.  Duplicate slots in one call give an unspecified row.
  *
@@ -107,7 +111,8 @@ PKV_API int pkv_version(void);
  *   slot_mapping_dev int64 [num_tokens]: destination slot, or < 0 to skip.
  *   k_cache_dev, v_cache_dev  bf16 pools (layout above) of num_blocks blocks.
  *   head_dim       64 or 128.   block_size  8, 16, 32, 64 or 128.
- *   rope_theta     RoPE base (> 0), e.g. 1e6 for Qwen3.
+ *   rope_theta     RoPE base, finite and > 0 (any value above 1e-280), e.g. 1e6 for Qwen3;
+ *                  else PKV_ERR_SHAPE.
  * num_tokens == 0 is a no-op returning PKV_OK.
  */
 PKV_API int pkv_kv_append(void* q_dev, int64_t q_stride_token, int64_t q_stride_head,
@@ -142,6 +147,18 @@ PKV_API int pkv_kv_append_paged(void* q_dev, int64_t q_stride_token, int64_t q_s
                                 int64_t head_dim, int64_t num_blocks, int64_t block_size,
                                 double rope_theta, int64_t* positions_out_dev,
                                 int64_t* slot_mapping_out_dev, void* stream);
+
+/*
+ * pkv_rope_turn_table -- the rotation frequencies pkv_kv_append uses, computed on the host (no
+ * GPU, no CUDA call): out[i], i < head_dim / 2, is f_i / (2 pi) modulo 1 as a 0.64 fixed-point
+ * fraction of a turn, f_i = rope_theta^(-2i / head_dim) evaluated with the C library's pow in
+ * fp64, i.e. round(frac(f_i / (2 pi)) * 2^64) mod 2^64, within one unit.  A token at position
+ * p turns pair i by 2 pi ((p * out[i]) mod 2^64) / 2^64 radians.  ("mini_engine" README, "What
+ * it does": RoPE.)  out holds head_dim / 2 values, owned by the caller.  Returns PKV_ERR_NULL
+ * for a NULL out, PKV_ERR_UNSUPPORTED for head_dim outside {64, 128}, PKV_ERR_SHAPE for a
+ * theta pkv_kv_append refuses.
+ */
+PKV_API int pkv_rope_turn_table(double rope_theta, int64_t head_dim, uint64_t* out);
 
 /*
  * pkv_paged_attention_workspace_size -- bytes of device workspace pkv_paged_attention needs
@@ -288,6 +305,19 @@ PKV_API int pkv_set_prefill_kernel(int kind);
 #define PKV_KERNEL_PREFILL 3
 #define PKV_KERNEL_DECODE 4
 PKV_API int pkv_set_kernel_events(int which, void* start_event, void* stop_event);
+
+/*
+ * pkv_set_fault_injection -- TEST ONLY: makes later pkv_paged_attention calls exercise the
+ * bounded waits inside the kernels (failure detection without a GPU fault).  kind 0 (default)
+ * turns it off.  PKV_FAULT_DECODE_NO_COPIES: the tensor-core decode kernel's producer warp
+ * issues no copy and no barrier arrival, so every consumer wait of a CTA with work runs out
+ * after about 2^31 SM clocks (about one second), sets PKV_DEVERR_TIMEOUT in the error word
+ * and the CTA finishes without further waits; nothing is left in flight and the context
+ * stays usable.  The decode rows of such a call are unspecified.  Process-wide.  Returns
+ * PKV_ERR_SHAPE for another kind.
+ */
+#define PKV_FAULT_DECODE_NO_COPIES 1
+PKV_API int pkv_set_fault_injection(int kind);
 
 /*
  * pkv_copy -- copy `bytes` from `src` to `dst` with a kernel on `stream` (no function of the

@@ -28,6 +28,7 @@ SIGNATURES = {
         [_c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_p,
          _c_i64, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_double, _c_p, _c_p, _c_p],
     ),
+    "pkv_rope_turn_table": (ctypes.c_int, [ctypes.c_double, _c_i64, ctypes.POINTER(ctypes.c_uint64)]),
     "pkv_paged_attention_workspace_size": (ctypes.c_size_t, [_c_i64] * 6),
     "pkv_paged_attention": (
         ctypes.c_int,
@@ -41,6 +42,7 @@ SIGNATURES = {
          _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_float, _c_p],
     ),
     "pkv_set_decode_ctas": (ctypes.c_int, [ctypes.c_int32]),
+    "pkv_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_overlap": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_decode_kernel": (ctypes.c_int, [ctypes.c_int]),
     "pkv_set_prefill_kernel": (ctypes.c_int, [ctypes.c_int]),

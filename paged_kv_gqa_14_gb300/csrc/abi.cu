@@ -1,6 +1,7 @@
 // C entry points declared in include/pkv.h: argument validation, workspace carving,
 // the per-device error word, dispatch to the kernel launchers.
 #include <atomic>
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 
@@ -22,6 +23,7 @@ std::atomic<int> g_decode_ctas_override{0};
 std::atomic<int> g_decode_kernel{0};
 std::atomic<int> g_prefill_kernel{0};
 std::atomic<int> g_overlap{1};
+std::atomic<int> g_fault{0};
 SideStream g_side[kMaxDevices];
 std::mutex g_side_lock[kMaxDevices];
 constexpr int kNumKernels = 5;
@@ -55,6 +57,12 @@ bool device_setup(int dev) {
   return g_err_ptr[dev] != nullptr && g_sm_count[dev] > 0;
 }
 
+// A RoPE base whose frequency table builds: finite, positive, and not so small that the
+// largest frequency (below 1 / theta for theta < 1) times 2^64 / (2 pi) overflows a double.
+bool rope_theta_ok(double theta) {
+  return theta > 0.0 && std::isfinite(theta) && (theta >= 1.0 || std::isfinite(2.9358905032820014e+18 / theta));
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Rows (t, h) of length d at offsets t*st + h*sh never overlap: token-major or head-major.
@@ -81,6 +89,8 @@ void record_kernel_event(int which, bool after, cudaStream_t stream) {
 int decode_kernel_choice() { return g_decode_kernel.load(); }
 
 int overlap_choice() { return g_overlap.load(); }
+
+int fault_injection_choice() { return g_fault.load(); }
 
 bool side_stream_for_device(SideStream* s) {
   const int dev = current_device();
@@ -130,6 +140,12 @@ int pkv_set_overlap(int on) {
   return PKV_OK;
 }
 
+int pkv_set_fault_injection(int kind) {
+  if (kind != 0 && kind != PKV_FAULT_DECODE_NO_COPIES) return PKV_ERR_SHAPE;
+  g_fault.store(kind);
+  return PKV_OK;
+}
+
 int pkv_set_decode_ctas(int32_t ctas) {
   if (ctas < 0) return PKV_ERR_SHAPE;
   g_decode_ctas_override.store(ctas);
@@ -171,7 +187,7 @@ int pkv_kv_append(void* q, int64_t q_st, int64_t q_sh, const void* k, int64_t k_
   const int bs_log2 = block_size_log2(block_size);
   if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
   if (num_blocks > INT32_MAX) return PKV_ERR_SHAPE;  // block ids are int32
-  if (!(rope_theta > 0.0)) return PKV_ERR_SHAPE;
+  if (!rope_theta_ok(rope_theta)) return PKV_ERR_SHAPE;
   if (num_tokens == 0) return PKV_OK;
   if (!q || !k || !v || !positions || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_NULL;
   if (q_st < 0 || q_sh < 0 || k_st < 0 || k_sh < 0 || v_st < 0 || v_sh < 0) return PKV_ERR_STRIDE;
@@ -220,7 +236,7 @@ int pkv_kv_append_paged(void* q, int64_t q_st, int64_t q_sh, const void* k, int6
   const int bs_log2 = block_size_log2(block_size);
   if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
   if (num_blocks > INT32_MAX) return PKV_ERR_SHAPE;  // block ids are int32
-  if (!(rope_theta > 0.0)) return PKV_ERR_SHAPE;
+  if (!rope_theta_ok(rope_theta)) return PKV_ERR_SHAPE;
   if (num_seqs > (1 << 30)) return PKV_ERR_SHAPE;
   if (num_tokens == 0) return PKV_OK;
   if (!q || !k || !v || !block_tables || !context_lens || !query_start_loc || !k_cache || !v_cache)
@@ -262,6 +278,15 @@ int pkv_kv_append_paged(void* q, int64_t q_st, int64_t q_sh, const void* k, int6
   a.theta = rope_theta;
   a.err = g_err_ptr[dev];
   return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_rope_turn_table(double rope_theta, int64_t head_dim, uint64_t* out) {
+  if (!out) return PKV_ERR_NULL;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  unsigned long long F[kMaxHeadDim / 2];
+  if (!rope_turn_table(rope_theta, static_cast<int>(head_dim), F)) return PKV_ERR_SHAPE;
+  for (int64_t i = 0; i < head_dim / 2; ++i) out[i] = F[i];
+  return PKV_OK;
 }
 
 size_t pkv_paged_attention_workspace_size(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads,
@@ -334,6 +359,7 @@ int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k
   a.decode_kernel = decode_kernel_choice();
   a.prefill_kernel = prefill_kernel_choice();
   a.overlap = overlap_choice();
+  a.fault = fault_injection_choice();
   a.plan = plan_view(workspace, ps);
   a.max_tiles = ps.max_tiles;
   a.err = g_err_ptr[dev];

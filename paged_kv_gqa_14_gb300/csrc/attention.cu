@@ -318,15 +318,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 template <int D, int G>
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   using C = DecodeCfg<D, G>;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_splitk_kernel<D, G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  if (const cudaError_t e = set_smem_once<decode_splitk_kernel<D, G>>(C::kSmemBytes); e != cudaSuccess) return e;
   DecodeParams p;
   p.q = static_cast<const bf16*>(a.q);
   p.q_st = a.q_st;
@@ -347,6 +339,7 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   p.qscale = a.scale * 1.4426950408889634f;
   p.plan = a.plan;
   p.err = a.err;
+  p.fault_no_copies = 0;
   record_kernel_event(PKV_KERNEL_DECODE, false, stream);
   const cudaError_t e = launch_pdl(decode_splitk_kernel<D, G>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
                                    C::kSmemBytes, stream, p);
@@ -402,15 +395,7 @@ int64_t prefill_tc_grid(const AttnArgs& a, int prows) {
 template <int D>
 cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaStream_t stream, bool pdl) {
   using C = PrefillTcCfg<D>;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  if (const cudaError_t e = set_smem_once<prefill_tc_kernel<D>>(C::kSmemBytes); e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(prefill_tc_grid(a, P.prows));
   record_kernel_event(PKV_KERNEL_PREFILL, false, stream);
   const cudaError_t e = launch_kernel(pdl, prefill_tc_kernel<D>, dim3(grid), dim3(256), C::kSmemBytes, stream, P);

@@ -41,7 +41,10 @@ extern "C" PKV_API int pkv_copy(void* dst, const void* src, size_t bytes, void* 
   const int64_t want = (n16 + kCopyThreads - 1) / kCopyThreads;
   const int64_t cap = static_cast<int64_t>(sms) * 4;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  copy_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  // the launch's own status (not cudaGetLastError, which would also report, and clear, an
+  // error left by unrelated earlier work)
+  const cudaError_t e = launch_kernel(false, copy_kernel, dim3(grid), dim3(kCopyThreads), 0,
+                                      static_cast<cudaStream_t>(stream), static_cast<uint4*>(dst),
+                                      static_cast<const uint4*>(src), n16);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -43,6 +43,7 @@ struct DecodeParams {
   float qscale;  // softmax scale * log2(e)
   Plan plan;
   unsigned int* err;
+  int fault_no_copies;  // test-only: the tensor-core decode's producer issues nothing
 };
 
 template <int D, int G>

@@ -22,15 +22,7 @@ constexpr int BS = PKV_DECODE_TC_BS;
 template <int D, int G>
 cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   using C = DecodeTcCfg<D, G>;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  if (const cudaError_t e = set_smem_once<decode_tc_kernel<D, G, BS>>(C::kSmemBytes); e != cudaSuccess) return e;
   DecodeTcParams P;
   if (!make_pool_map_heads(&P.tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, D) ||
       !make_pool_map_heads(&P.tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, D))
@@ -55,6 +47,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   p.qscale = a.scale * 1.4426950408889634f;
   p.plan = a.plan;
   p.err = a.err;
+  p.fault_no_copies = a.fault == PKV_FAULT_DECODE_NO_COPIES;
   record_kernel_event(PKV_KERNEL_DECODE, false, stream);
   const cudaError_t e = launch_pdl(decode_tc_kernel<D, G, BS>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
                                    C::kSmemBytes, stream, P);

@@ -157,6 +157,9 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
 
   if (warp == kDecodeWarps) {
     // ------------------------------------------------------------------ producer warp
+    // Fault injection for the tests of the bounded waits: no copy and no arrival is issued,
+    // so the consumers' first waits run out, set PKV_DEVERR_TIMEOUT and the CTA finishes.
+    if (p.fault_no_copies) return;
     const uint64_t pol = l2_policy_evict_first();
     // lane -> (K or V, page, 64-dim half) of the unit's boxes; 2 P HALVES <= 32 boxes
     const int per_kv = pps * HALVES;

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace pkv {
 
 // The kernels walk a sequence's keys in pages of 16 tokens whatever the pool's block size:
@@ -94,6 +96,10 @@ struct AppendArgs {
   unsigned int* err;
 };
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+// The kv_append rotation frequencies as 0.64 fixed-point turn fractions F[0 .. head_dim/2);
+// false for a theta that is not finite and positive, whose table does not build, or a head_dim
+// outside {64, 128}.
+bool rope_turn_table(double theta, int head_dim, unsigned long long* F);
 
 struct AttnArgs {
   const void* q;
@@ -116,6 +122,7 @@ struct AttnArgs {
   int decode_kernel;   // 0 automatic, 1 CUDA-core (warp-shuffle), 2 tensor-core (mma.sync)
   int prefill_kernel;  // 1 mma.sync tiles, 2 tcgen05 tiles (resolved from the process setting)
   int overlap;         // 1: prefill tiles run beside the decode on a second stream (SMs split)
+  int fault;           // test-only fault injection (pkv_set_fault_injection); 0 in normal use
   Plan plan;
   int64_t max_tiles;
   unsigned int* err;
@@ -194,11 +201,29 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return launch_kernel(true, kernel, grid, block, smem, stream, static_cast<Args&&>(args)...);
 }
 
+// Raises `Kernel`'s dynamic shared-memory limit to `bytes`, once per device (thread-safe:
+// std::call_once); later calls return the status of that one attribute call.
+template <auto Kernel>
+cudaError_t set_smem_once(int bytes) {
+  constexpr int kDevices = 64;
+  static std::once_flag once[kDevices];
+  static cudaError_t status[kDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kDevices) return cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::call_once(once[dev], [bytes, dev] {
+    status[dev] = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+  return status[dev];
+}
+
 // Records the caller's timing event around a kernel launch when one is registered
 // (pkv_set_kernel_events); `after` selects the stop event.
 void record_kernel_event(int which, bool after, cudaStream_t stream);
 int decode_ctas_for_device();
 int decode_kernel_choice();
+int fault_injection_choice();
 int prefill_kernel_choice();
 
 }  // namespace pkv

@@ -6,11 +6,20 @@
 // One CTA per new token.  Its q, k and v rows are read first (their addresses do not
 // depend on the position), then the d/2 rotation angles are computed once into shared
 // memory: angle = pos * f_i with f_i = theta^(-2i/d) (fp64 on the host), taken modulo one
-// turn exactly in 64-bit integer arithmetic (RopeFreqs), then sincosf in fp32.  Every head
-// of q (in place) and k (into the slot) is rotated pairwise (i, i + d/2) in fp32 and rounded
-// to bf16 nearest-even; v is a 16-byte vector copy.  All global accesses are 16-byte
-// vectors along head_dim.
+// turn exactly in 64-bit integer arithmetic (RopeFreqs), split exactly into a quarter turn
+// and a remainder in [-pi/4, pi/4) that reaches fp32 with one rounding, then sincosf in fp32
+// and an exact quarter-turn swap.  Every head of q (in place) and k (into the slot) is
+// rotated pairwise (i, i + d/2) in fp32 and rounded to bf16 nearest-even; v is a 16-byte
+// vector copy.  All global accesses are 16-byte vectors along head_dim.
+//
+// Error of a rotated fp32 value before its bf16 rounding, for a pair (x, y) at a position
+// below 2^31: the fp32 remainder angle is within 2^-25 rad of the exact one (one rounding at
+// |r| < 1), plus pos * 2 pi / 2^64 from the rounding of F_i; sincosf is within 2 ulp (2^-23)
+// of sin and cos; the two products and the difference add at most 2^-23 (|x| + |y|).  In
+// all, |error| <= 2.7e-7 (|x| + |y|), below 2^-21 (|x| + |y|).
 #include <math.h>
+
+#include <cmath>
 
 #include "common.cuh"
 #include "internal.h"
@@ -40,16 +49,44 @@ struct AppendSrc {
 };
 
 // The rotation frequencies as fractions of a turn in 0.64 fixed point:
-// F_i = round(f_i / (2 pi) * 2^64), f_i = theta^(-2i/d).  The angle of position p is then
-// p f_i = 2 pi (p F_i / 2^64), and its part modulo one turn is the low 64 bits of the integer
-// product p F_i: exact up to the rounding of F_i (at most p / 2^64 of a turn), with no
-// floating-point range reduction.
+// F_i = round(frac(f_i / (2 pi)) * 2^64), f_i = theta^(-2i/d).  The angle of position p is
+// then p f_i = 2 pi (p F_i / 2^64) modulo whole turns, and its part modulo one turn is the
+// low 64 bits of the integer product p F_i: exact up to the rounding of F_i (at most p / 2^64
+// of a turn), with no floating-point range reduction.
 struct RopeFreqs {
   unsigned long long F[kMaxHeadDim / 2];
 };
 
-// 2 pi / 2^32: radians per unit of the top 32 bits of a 0.64 fixed-point turn.
-constexpr float kTwoPiOver2p32 = 1.4629180792671596e-09f;
+// 2 pi / 2^32 (radians per unit of the top 32 bits of a 0.64 fixed-point turn) as the sum of
+// two floats: hi the float nearest to it, lo the float nearest to the rest.
+constexpr float kTwoPiOver2p32Hi = 1.4629180792671596e-09f;
+constexpr float kTwoPiOver2p32Lo =
+    static_cast<float>(1.4629180792671596e-09 - static_cast<double>(kTwoPiOver2p32Hi));
+
+// cos and sin of the angle 2 pi turn / 2^64.  The nearest quarter turn k = round(4 turn / 2^64)
+// mod 4 and the remainder rem = turn - k 2^62, a signed integer in [-2^61, 2^61], are exact;
+// r = 2 pi rem / 2^64 in [-pi/4, pi/4] is formed from rem's top word (rounded to a float, the
+// rounding kept as a small exact integer), its low word and the two-float constant, with one
+// fp32 rounding in the last step.  (cos, sin) of k pi/2 + r are (cos r, sin r) turned by k
+// quarter turns: a swap and sign changes, exact.
+__device__ __forceinline__ float2 cos_sin_of_turn(unsigned long long turn) {
+  const unsigned k = static_cast<unsigned>((turn + (1ull << 61)) >> 62);  // 0..3, wraps mod 4
+  const long long rem = static_cast<long long>(turn - (static_cast<unsigned long long>(k) << 62));
+  const int hi = static_cast<int>(rem >> 32);  // |hi| <= 2^29
+  const unsigned lo = static_cast<unsigned>(rem);
+  const float hi_f = static_cast<float>(hi);
+  const int hi_rest = hi - static_cast<int>(hi_f);  // exact, |hi_rest| <= 16
+  const float x_lo = fmaf(static_cast<float>(lo), 2.3283064365386963e-10f /* 2^-32 */, static_cast<float>(hi_rest));
+  const float r = fmaf(hi_f, kTwoPiOver2p32Hi, fmaf(hi_f, kTwoPiOver2p32Lo, x_lo * kTwoPiOver2p32Hi));
+  float s, c;
+  sincosf(r, &s, &c);
+  switch (k & 3u) {
+    case 0: return make_float2(c, s);
+    case 1: return make_float2(-s, c);
+    case 2: return make_float2(-c, -s);
+    default: return make_float2(s, -c);
+  }
+}
 
 __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float2* cs) {
   uint32_t* a = reinterpret_cast<uint32_t*>(&lo);
@@ -191,14 +228,9 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendThreads == 64 ? 16 : kA
   const int64_t pos = s_pos;
   const int64_t slot = s_slot;
 
-  for (int i = tid; i < HALF; i += kAppendThreads) {
-    // the token's angle modulo one turn, as a signed fraction of a turn: r in [-pi, pi)
-    const unsigned long long turn = static_cast<unsigned long long>(pos) * fr.F[i];
-    const float r = static_cast<float>(static_cast<int>(turn >> 32)) * kTwoPiOver2p32;
-    float sn, cn;
-    sincosf(r, &sn, &cn);
-    cs[i] = make_float2(cn, sn);
-  }
+  // the token's angles modulo one turn: pos F_i mod 2^64 in 0.64 fixed point
+  for (int i = tid; i < HALF; i += kAppendThreads)
+    cs[i] = cos_sin_of_turn(static_cast<unsigned long long>(pos) * fr.F[i]);
   const bool in_range = slot < num_slots;
   const bool write_kv = slot >= 0 && in_range;
   if (!in_range && tid == 0) raise_error(err, PKV_DEVERR_SLOT_RANGE);
@@ -259,27 +291,43 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendThreads == 64 ? 16 : kA
 
 namespace {
 
-// round(f / (2 pi) * 2^64) for 0 <= f <= 1, with 2^64 / (2 pi) as a double-double
-// (hi + lo) and the product's rounding error recovered by an FMA, so F is within one unit.
-unsigned long long turn_fraction_0p64(double f) {
+// round(frac(f / (2 pi)) * 2^64) for f > 0, to within one unit: 2^64 / (2 pi) is a double-double
+// (kHi + kLo), the product's rounding error is recovered by an FMA, and whole turns drop out
+// modulo 2^64 through an exact fmod, so f above one turn per position (rope_theta < 1) is
+// reduced as exactly as f below.  False when f * 2^64 / (2 pi) is not finite.
+bool turn_fraction_0p64(double f, unsigned long long* out) {
   constexpr double kHi = 2.9358905032820014e+18;  // 2^64 / (2 pi) = kHi + kLo
   constexpr double kLo = -181.50375616818445;
+  constexpr double kTwo64 = 18446744073709551616.0;
   const double p = f * kHi;
+  if (!std::isfinite(p) || !(f >= 0.0)) return false;
   const double e = fma(f, kHi, -p) + f * kLo;  // f (kHi + kLo) - p
-  const double whole = floor(p);
-  return static_cast<unsigned long long>(static_cast<long long>(whole)) +
-         static_cast<unsigned long long>(llround((p - whole) + e));
+  const double pm = fmod(p, kTwo64);           // exact, in [0, 2^64)
+  const double whole = floor(pm);
+  *out = static_cast<unsigned long long>(whole) + static_cast<unsigned long long>(llround((pm - whole) + e));
+  return true;
 }
 
-// The frequency table of the last (theta, head_dim) seen by this host thread.
+}  // namespace
+
+bool rope_turn_table(double theta, int head_dim, unsigned long long* F) {
+  if (!(theta > 0.0) || !std::isfinite(theta) || (head_dim != 64 && head_dim != 128)) return false;
+  for (int i = 0; i < head_dim / 2; ++i)
+    if (!turn_fraction_0p64(pow(theta, -2.0 * i / head_dim), &F[i])) return false;
+  return true;
+}
+
+namespace {
+
+// The frequency table of the last (theta, head_dim) seen by this host thread (validated by
+// the entry points, which refuse a theta whose table does not build).
 const RopeFreqs& rope_freqs(double theta, int head_dim) {
   thread_local RopeFreqs table;
   thread_local double t_theta = -1.0;
   thread_local int t_dim = -1;
   if (theta != t_theta || head_dim != t_dim) {
-    const int half = head_dim / 2;
-    for (int i = 0; i < kMaxHeadDim / 2; ++i)
-      table.F[i] = i < half ? turn_fraction_0p64(pow(theta, -2.0 * i / head_dim)) : 0ull;
+    for (int i = 0; i < kMaxHeadDim / 2; ++i) table.F[i] = 0ull;
+    rope_turn_table(theta, head_dim, table.F);
     t_theta = theta;
     t_dim = head_dim;
   }

@@ -333,15 +333,7 @@ inline int64_t prefill_mma_grid(const AttnArgs& a) {
 template <int D>
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream, bool pdl) {
   using C = PrefillCfg<D>;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  if (const cudaError_t e = set_smem_once<prefill_kernel<D>>(C::kSmemBytes); e != cudaSuccess) return e;
   const PrefillParams p = make_prefill_params(a);
   const unsigned grid = static_cast<unsigned>(prefill_mma_grid(a));
   if (grid == 0) return cudaSuccess;

@@ -129,6 +129,16 @@ def kv_append_paged(q, k, v, block_tables, context_lens, query_start_loc, k_cach
     _lib.check("pkv_kv_append_paged", st)
 
 
+def rope_turn_table(rope_theta, head_dim):
+    """The rotation frequencies kv_append uses, as uint64 0.64 fixed-point turn fractions
+    (``pkv_rope_turn_table``; host only, no GPU)."""
+    import numpy as np
+
+    out = (ctypes.c_uint64 * (int(head_dim) // 2 or 1))()
+    _lib.check("pkv_rope_turn_table", _lib.load().pkv_rope_turn_table(float(rope_theta), int(head_dim), out))
+    return np.frombuffer(out, dtype=np.uint64)[: int(head_dim) // 2].copy()
+
+
 def workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq):
     """Bytes of workspace ``paged_attention`` needs (``pkv_paged_attention_workspace_size``)."""
     n = _lib.load().pkv_paged_attention_workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads,
@@ -211,6 +221,13 @@ PREFILL_KERNELS = {"auto": 0, "mma": 1, "tcgen05": 2}
 def set_prefill_kernel(kind):
     """Prefill-tile arithmetic for later calls: "auto", "mma" (mma.sync) or "tcgen05"."""
     _lib.check("pkv_set_prefill_kernel", _lib.load().pkv_set_prefill_kernel(PREFILL_KERNELS[kind]))
+
+
+def set_fault_injection(kind):
+    """Test only: ``"decode_no_copies"`` makes the decode producer issue nothing, so its
+    consumers' bounded waits run out (``pkv_set_fault_injection``); ``None`` turns it off."""
+    code = {None: 0, "decode_no_copies": 1}[kind]
+    _lib.check("pkv_set_fault_injection", _lib.load().pkv_set_fault_injection(code))
 
 
 def get_device_error(clear=True, stream=None):

@@ -83,11 +83,18 @@ def ulp_bf16(x):
 def rope_tol(x_bits, ref):
     """Allowed |gpu - oracle| for a rotated bf16 value.
 
-    The kernel rotates in fp32 (x cos a - y sin a with sincosf, a few fp32 roundings, error
-    well below 2^-21 (|x| + |y|)) and rounds once to bf16.  Where the result is not tiny that
-    moves the bf16 value by at most one ulp (only near rounding ties); where x cos a and
-    y sin a cancel, the fp32 absolute error can exceed an ulp of the tiny result.  Bound:
-    one bf16 ulp of the reference plus 2^-21 times the pair's magnitude |x_i| + |x_{i+d/2}|.
+    Error budget of the kernel's fp32 value before its bf16 rounding, for a pair (x, y) at a
+    position p < 2^31 (both sides start from the same bf16 inputs and the same fp64 f_i):
+      * angle: the 0.64 fixed-point turn p F_i mod 2^64 is exact up to F_i's rounding
+        (p 2 pi / 2^64 rad); the quarter turn is exact; the remainder r in [-pi/4, pi/4]
+        reaches fp32 with one rounding, <= 2^-25 rad;
+      * sincosf: <= 2 ulp, i.e. <= 2^-23 absolute on values in [-1, 1];
+      * x c - y s: one product rounding and one sum rounding, <= 2^-23 (|x| + |y|);
+    so |fp32 - exact| <= (2^-23 + 2^-25 + 2^-23) (|x| + |y|) < 2.7e-7 (|x| + |y|) for the
+    positions tested (p 2 pi 2^-64 < 1e-11 for p <= 2^24).  The oracle's own fp64 angle p f_i
+    carries p f_i 2^-53 rad (below 2^-28 here).  Rounding both to bf16 then differs by at most
+    that error plus one bf16 ulp, so the bound is one ulp of the reference plus
+    2^-21 (|x_i| + |x_{i+d/2}|), which holds the derived 2.7e-7 with a margin of 1.7.
     """
     x = np.abs(np.asarray(x_bits_to_f64(x_bits)))
     half = x.shape[-1] // 2

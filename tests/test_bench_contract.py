@@ -59,3 +59,40 @@ def test_small_workloads_are_timed_with_an_l2_flush(index):
     bt = W.config(index, poison=False)
     assert bench.kv_unique_bytes(bt) < 2 * bench.L2_BYTES
     assert bench.FLUSH_BYTES >= 2 * bench.L2_BYTES
+
+
+def test_gpu_count_must_match_the_launched_processes():
+    # without torchrun there is one process: --gpus 2 is refused instead of printing n_gpus 1
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                          "--workload", "1"], capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
+    assert out.returncode != 0 and "--gpus 2 but 1 process" in out.stderr
+
+
+def test_prefill_flops_count_unmasked_pairs():
+    # a 3-row span over 5 keys sees 3 + 4 + 5 keys; decode rows are not counted
+    from paged_kv_gqa_14_gb300 import workloads as W
+
+    bt = W.make_batch([5, 9], [3, 1], 4, 2, 64, 4, seed=0)
+    assert bench.prefill_flops(bt) == 4 * 64 * 4 * (3 + 4 + 5)
+    # the mixed workload: 2,098,176 pairs per head x 16 heads x 4 x 128
+    bt5 = W.config(5, poison=False)
+    assert bench.prefill_flops(bt5) == 2_098_176 * 16 * 4 * 128
+
+
+def test_traffic_record_is_read_back_only_for_the_same_sources(tmp_path, monkeypatch):
+    csv = tmp_path / "cap.csv"
+    csv.write_text(
+        '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size",'
+        '"Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n'
+        '"3","1","p","h","void pkv::decode_tc_kernel<128, 2, 16>(pkv::DecodeTcParams)","1","7","(288, 1, 1)",'
+        '"(152, 1, 1)","0","10.3","m","dram__bytes_read.sum","byte","1,000"\n'
+        '"3","1","p","h","void pkv::decode_tc_kernel<128, 2, 16>(pkv::DecodeTcParams)","1","7","(288, 1, 1)",'
+        '"(152, 1, 1)","0","10.3","m","dram__bytes_write.sum","Kbyte","2"\n')
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "traffic.json"))
+    rec = bench.record_traffic(str(csv), "decode", "w3", "ncu ...")
+    assert rec["dram_bytes_per_launch"] == 3000 and rec["launches"] == 1
+    assert bench.kernel_traffic("decode", "w3") == 3000.0
+    assert bench.kernel_traffic("decode", "other") is None
+    monkeypatch.setattr(bench, "source_sha256", lambda: "changed")
+    assert bench.kernel_traffic("decode", "w3") is None

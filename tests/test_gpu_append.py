@@ -51,10 +51,12 @@ def test_append_matches_oracle_on_workloads(index):
     assert frac_off < 0.01  # 1-ulp differences are rare rounding ties, not a pattern
 
 
-@pytest.mark.parametrize("d,theta", [(128, 1.0e6), (64, 1.0e4)])
+@pytest.mark.parametrize("d,theta", [(128, 1.0e6), (64, 1.0e4), (64, 0.5), (128, 0.1)])
 def test_append_large_positions(d, theta):
     # positions up to 2^24: the kernel takes each angle modulo one turn in 64-bit fixed point;
-    # the oracle's fp64 angle is exact to 2^-28 rad there, well inside the rotation tolerance
+    # the oracle's fp64 angle is exact to p f_i 2^-53 rad there (2^-28 for f_i <= 1; a base
+    # below one turns a pair by up to 1 / theta rad per position: under 2^-25 at theta 0.1), well
+    # inside the rotation tolerance
     bt = W.make_batch([3] * 16, [1] * 16, 16, 8 if d == 128 else 4, d, 20, seed=21, rope_theta=theta)
     bt.positions = np.array([0, 1, 2, 31, 999, 1000, 65535, 65536, 123457, 1_000_003, 4_000_037,
                              2**22 + 3, 7_777_777, 2**23 - 1, 2**24 - 5, 2**24], dtype=np.int64)

@@ -340,3 +340,84 @@ def test_prefill_beside_decode_matches_serial_order(case, overlap_setting):
     rows = np.concatenate([np.arange(qsl[b], qsl[b + 1]) for b in range(bt.num_seqs) if qsl[b + 1] - qsl[b] > 1])
     assert len(rows) > 0
     assert np.array_equal(outs[True][rows], outs[False][rows])
+
+
+def _visible_rows(bt):
+    """(row, sequence, last visible key) for every row a span covers."""
+    out = []
+    qsl, ctx = bt.query_start_loc, bt.context_lens
+    for b in range(bt.num_seqs):
+        n = int(qsl[b + 1] - qsl[b])
+        for r in range(n):
+            out.append((int(qsl[b]) + r, b, int(ctx[b]) - n + r))
+    return out
+
+
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
+def test_zero_query_gives_mean_of_visible_values(prefill_kernel):
+    # q = 0: every visible key scores 0, so each row is the plain mean of the V rows it sees
+    # (a decode row: the whole context; prefill row r of n: keys 0 .. ctx - n + r), on both
+    # the decode and the prefill kernels, across page and tile boundaries
+    ctx, spans = [1, 17, 300, 140, 64, 2100], [1, 1, 1, 40, 64, 300]
+    pages = sum(-(-c // 16) for c in ctx)
+    bt = W.make_batch(ctx, spans, 16, 8, 128, pages + 4, seed=41)
+    _, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
+                                 bt.rope_theta)
+    q0 = np.zeros_like(bt.q)
+    got, _ = _attend_oracle_inputs(bt, q0, kc, vc)
+    G = bt.num_q_heads // bt.num_kv_heads
+    ref = np.empty_like(got, dtype=np.float64)
+    for row, b, last in _visible_rows(bt):
+        _, V = oracle.gather_sequence_kv(kc, vc, bt.block_tables[b], int(bt.context_lens[b]))
+        mean = V[: last + 1].mean(axis=0)  # [Hkv, d]
+        ref[row] = np.repeat(mean, G, axis=0)
+    assert_close(got, ref, f"q = 0, prefill={prefill_kernel}")
+
+
+def test_outputs_lie_in_the_convex_hull_of_visible_values():
+    # a softmax-weighted average: every output coordinate lies between the smallest and the
+    # largest value of that V column over the keys the row sees (up to the bf16 rounding of the
+    # output and fp32 accumulation: one bf16 ulp of the bound plus 1e-3)
+    bt, q_rot, kc, vc, _ = config_with_oracle(5)
+    got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    G = bt.num_q_heads // bt.num_kv_heads
+    cache = {}
+    worst = 0.0
+    for row, b, last in _visible_rows(bt):
+        if b not in cache:
+            cache[b] = oracle.gather_sequence_kv(kc, vc, bt.block_tables[b], int(bt.context_lens[b]))[1]
+        V = cache[b][: last + 1]
+        lo = np.repeat(V.min(axis=0), G, axis=0)
+        hi = np.repeat(V.max(axis=0), G, axis=0)
+        slack = 1e-3 + np.maximum(np.abs(lo), np.abs(hi)) * 2.0**-8
+        worst = max(worst, float(np.max(lo - got[row])), float(np.max(got[row] - hi)))
+        assert np.all(got[row] >= lo - slack) and np.all(got[row] <= hi + slack), f"row {row}"
+    assert worst <= 1e-2
+
+
+def test_bounded_wait_runs_out_and_reports_timeout():
+    # failure detection without a GPU fault: with the test-only fault injection the decode's
+    # producer warp issues no copy and no barrier arrival, so its consumers' bounded waits run
+    # out (about 2^31 SM clocks); the kernel sets PKV_DEVERR_TIMEOUT and finishes with nothing
+    # in flight, and the next call on the same context is correct again
+    import time
+
+    bt, q_rot, kc, vc, ref = config_with_oracle(1)
+    d = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
+    d.attend()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    ops.set_fault_injection("decode_no_copies")
+    try:
+        t0 = time.perf_counter()
+        d.attend()
+        torch.cuda.synchronize()
+        waited = time.perf_counter() - t0
+    finally:
+        ops.set_fault_injection(None)
+    assert ops.get_device_error() == 0x10  # PKV_DEVERR_TIMEOUT, nothing else
+    assert 0.2 < waited < 60.0
+    got = d.attend().float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    assert_close(got, ref, "after a timed-out call")
