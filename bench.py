@@ -709,7 +709,7 @@ def main():
                     help="tokens per pool block (the workload keeps its pool size in tokens)")
     ap.add_argument("--seqs", type=int, default=0, help="only the first N sequences (small profiling case)")
     ap.add_argument("--decode-kernel", choices=["auto", "simt", "tensor"], default="auto")
-    ap.add_argument("--prefill-kernel", choices=["auto", "mma", "tcgen05", "tcgen05x2"], default="auto")
+    ap.add_argument("--prefill-kernel", choices=["auto", "mma", "tcgen05"], default="auto")
     ap.add_argument("--no-overlap", action="store_true",
                     help="prefill tiles before the decode on one stream (default: beside it, SMs split)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -159,7 +159,7 @@ int pkv_set_decode_kernel(int kind) {
 }
 
 int pkv_set_prefill_kernel(int kind) {
-  if (kind < 0 || kind > 3) return PKV_ERR_SHAPE;
+  if (kind < 0 || kind > 2) return PKV_ERR_SHAPE;
   g_prefill_kernel.store(kind);
   return PKV_OK;
 }

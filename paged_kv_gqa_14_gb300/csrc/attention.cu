@@ -20,7 +20,6 @@
 #include "decode_tc.cuh"
 #include "prefill.cuh"
 #include "prefill_tc.cuh"
-#include "prefill_tc2.cuh"
 
 namespace pkv {
 
@@ -214,12 +213,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
           unsigned long long sum = 0;
           int mx = 0;
           for (int j = 0; j < v.c; ++j) {
-            int nk = ceil_div(ctx - span + min((j + 1) * tile_q, span), 128);
-            if (split.pair) {  // an item of two query tiles: the first half's key tiles too
-              const int half = tile_q / 2;
-              const int first = ceil_div(ctx - span + min(j * tile_q + half, span), 128);
-              nk = j * tile_q + half < span ? nk + first : first;
-            }
+            const int nk = ceil_div(ctx - span + min((j + 1) * tile_q, span), 128);
             sum += static_cast<unsigned long long>(nk);
             mx = max(mx, nk);
           }
@@ -391,30 +385,6 @@ bool make_prefill_tc_params(const AttnArgs& a, PrefillTcParams* P) {
   return true;
 }
 
-bool make_prefill_tc2_params(const AttnArgs& a, PrefillTc2Params* P) {
-  if (a.q_sh <= 0 || a.q_st <= 0) return false;
-  if (!make_q_map(&P->tmap_q, a) ||
-      !make_pool_map(&P->tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, a.head_dim) ||
-      !make_pool_map(&P->tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, a.head_dim))
-    return false;
-  P->p = make_prefill_params(a);
-  P->group = a.hq / a.hkv;
-  P->prows = kTcPrefillRows / P->group;
-  return true;
-}
-
-template <int D>
-cudaError_t launch_prefill_tc2(const AttnArgs& a, const PrefillTc2Params& P, int64_t grid, cudaStream_t stream,
-                               bool pdl) {
-  using C = PrefillTc2Cfg<D>;
-  if (const cudaError_t e = set_smem_once<prefill_tc2_kernel<D>>(C::kSmemBytes); e != cudaSuccess) return e;
-  record_kernel_event(PKV_KERNEL_PREFILL, false, stream);
-  const cudaError_t e = launch_kernel(pdl, prefill_tc2_kernel<D>, dim3(static_cast<unsigned>(grid)),
-                                      dim3(C::kThreads), C::kSmemBytes, stream, P);
-  record_kernel_event(PKV_KERNEL_PREFILL, true, stream);
-  return e;
-}
-
 // CTAs the tcgen05 prefill is launched with: one per SM, at most one per item.
 int64_t prefill_tc_grid(const AttnArgs& a, int prows) {
   const int64_t max_items = (a.num_tokens / prows + a.num_seqs + 1) * a.hkv;
@@ -454,22 +424,17 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   // prefill arithmetic: tcgen05 (128-row tiles) when chosen and its q tensor map encodes,
   // else mma.sync (64-row tiles)
   PrefillTcParams tcp;
-  PrefillTc2Params tc2p;
-  const bool use_tc2 = a.prefill_kernel == 3 && make_prefill_tc2_params(a, &tc2p);
-  const bool use_tc = !use_tc2 && a.prefill_kernel >= 2 && make_prefill_tc_params(a, &tcp);
-  const int prows = kTcPrefillRows / (a.hq / a.hkv);
-  const int tile_q = use_tc2 ? 2 * prows : use_tc ? prows : kPrefillTileQ;
+  const bool use_tc = a.prefill_kernel == 2 && make_prefill_tc_params(a, &tcp);
+  const int tile_q = use_tc ? kTcPrefillRows / (a.hq / a.hkv) : kPrefillTileQ;
   const int sms = device_sm_count();
-  const int64_t pf_grid = use_tc2 ? prefill_tc_grid(a, 2 * prows) : use_tc ? prefill_tc_grid(a, prows)
-                                                                             : prefill_mma_grid(a);
+  const int64_t pf_grid = use_tc ? prefill_tc_grid(a, tcp.prows) : prefill_mma_grid(a);
   // Prefill beside the decode: only with spans of two or more tokens (more tokens than
   // sequences), the tcgen05 tiles (one CTA per SM) and the default one decode CTA per SM.
   SideStream side{};
-  const bool split = a.overlap && (use_tc || use_tc2) && a.num_tokens > a.num_seqs && a.decode_ctas == sms &&
-                     sms > 1 && side_stream_for_device(&side);
+  const bool split = a.overlap && use_tc && a.num_tokens > a.num_seqs && a.decode_ctas == sms && sms > 1 &&
+                     side_stream_for_device(&side);
   SplitArgs sp{};
   sp.on = split ? 1 : 0;
-  sp.pair = use_tc2 ? 1 : 0;
   sp.sms = sms;
   sp.pf_grid = static_cast<int>(pf_grid);
   sp.hkv = a.hkv;
@@ -477,7 +442,7 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   sp.tile_bytes = 128.f * a.head_dim * 4.f;
   sp.hbm = kSplitHbmBytesPerNs;
   sp.dec_sm = kSplitDecodeSmBytesPerNs;
-  sp.pf_sm = use_tc2 ? kSplitPrefillPairSmBytesPerNs : split_prefill_sm_bytes_per_ns(a.bs_log2);
+  sp.pf_sm = split_prefill_sm_bytes_per_ns(a.bs_log2);
   record_kernel_event(PKV_KERNEL_PLAN, false, stream);
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
                              static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps,
@@ -486,9 +451,6 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   record_kernel_event(PKV_KERNEL_PLAN, true, stream);
   if (e != cudaSuccess) return e;
   auto prefill = [&](cudaStream_t s, bool pdl) -> cudaError_t {
-    if (use_tc2)
-      return (a.head_dim == 128) ? launch_prefill_tc2<128>(a, tc2p, pf_grid, s, pdl)
-                                 : launch_prefill_tc2<64>(a, tc2p, pf_grid, s, pdl);
     if (use_tc)
       return (a.head_dim == 128) ? launch_prefill_tc<128>(a, tcp, s, pdl) : launch_prefill_tc<64>(a, tcp, s, pdl);
     return (a.head_dim == 128) ? launch_prefill<128>(a, s, pdl) : launch_prefill<64>(a, s, pdl);

@@ -155,13 +155,9 @@ constexpr float kSplitDecodeSmBytesPerNs = 58.f;
 // and 128-token blocks alike (the tile's TMA boxes grow with the block, the pace does not),
 // and 29 GB/s at 8-token blocks (two half-height boxes per page).
 inline float split_prefill_sm_bytes_per_ns(int bs_log2) { return bs_log2 <= 3 ? 29.f : 33.5f; }
-// The two-tile prefill's pace per SM: K/V bytes of one 128-key tile per 128 query rows
-// (a first estimate, to be replaced by the measured rate).
-constexpr float kSplitPrefillPairSmBytesPerNs = 70.f;
 
 struct SplitArgs {
   int on;             // 1: the planner splits `sms` CTAs between prefill and decode
-  int pair;           // 1: a prefill item holds two query tiles (tile_q positions, two halves)
   int sms;            // CTAs to share out (one per SM)
   int pf_grid;        // CTAs the prefill kernel is launched with
   int hkv;            // prefill items per q tile (one per kv head)

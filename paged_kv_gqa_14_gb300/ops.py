@@ -215,7 +215,7 @@ def set_decode_kernel(kind):
     _lib.check("pkv_set_decode_kernel", _lib.load().pkv_set_decode_kernel(DECODE_KERNELS[kind]))
 
 
-PREFILL_KERNELS = {"auto": 0, "mma": 1, "tcgen05": 2, "tcgen05x2": 3}
+PREFILL_KERNELS = {"auto": 0, "mma": 1, "tcgen05": 2}
 
 
 def set_prefill_kernel(kind):

@@ -90,14 +90,14 @@ def prefill_kernel(request):
     ops.set_prefill_kernel("auto")
 
 
-@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05", "tcgen05x2"], indirect=True)
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
 def test_both_prefill_kernels_on_mixed_workload(prefill_kernel):
     bt, q_rot, kc, vc, ref = config_with_oracle(5)
     got, _ = _attend_oracle_inputs(bt, q_rot, kc, vc)
     assert_close(got, ref, f"{bt.name} prefill={prefill_kernel}")
 
 
-@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05", "tcgen05x2"], indirect=True)
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
 @pytest.mark.parametrize("case", [
     ([300, 40, 129], [300, 40, 129], 16, 8, 128),     # from-scratch chunks: ragged q tiles
     ([1000, 700, 2], [260, 129, 2], 16, 8, 128),      # chunks over earlier context, tiny span
@@ -115,7 +115,7 @@ def test_both_prefill_kernels_on_long_chunks(prefill_kernel, case):
     assert_close(got, ref, f"prefill={prefill_kernel} ctx={ctx} spans={spans}")
 
 
-@pytest.mark.parametrize("prefill_kernel", ["tcgen05", "tcgen05x2"], indirect=True)
+@pytest.mark.parametrize("prefill_kernel", ["tcgen05"], indirect=True)
 @pytest.mark.parametrize("group", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("d", [64, 128])
 def test_tcgen05_prefill_every_group_size(prefill_kernel, group, d):
@@ -131,7 +131,7 @@ def test_tcgen05_prefill_every_group_size(prefill_kernel, group, d):
     assert_close(got, ref, f"G={group} d={d}")
 
 
-@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05", "tcgen05x2"], indirect=True)
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
 @pytest.mark.parametrize("seed", range(200, 210))
 def test_both_prefill_kernels_random_mixed(seed, prefill_kernel):
     bt = W.random_case(seed, max_seqs=5, max_ctx=500, head_dims=(64, 128), groups=(1, 2, 4, 7),
@@ -289,7 +289,7 @@ def test_cuda_graph_replay_matches_eager_step():
     assert_close(out.float().cpu().numpy(), ref, "graph replay")
 
 
-@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05", "tcgen05x2"], indirect=True)
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
 @pytest.mark.parametrize("bs", [16, 128])
 def test_long_contexts_and_largest_group(prefill_kernel, bs):
     # the largest shapes of the supported set: G = 8 (16 q / 2 kv heads), d 128, a 32768-token
@@ -353,7 +353,7 @@ def _visible_rows(bt):
     return out
 
 
-@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05", "tcgen05x2"], indirect=True)
+@pytest.mark.parametrize("prefill_kernel", ["mma", "tcgen05"], indirect=True)
 def test_zero_query_gives_mean_of_visible_values(prefill_kernel):
     # q = 0: every visible key scores 0, so each row is the plain mean of the V rows it sees
     # (a decode row: the whole context; prefill row r of n: keys 0 .. ctx - n + r), on both

@@ -39,7 +39,7 @@ def _expected(bt, decode_ctas, tile_q):
 
 
 @pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
-@pytest.mark.parametrize("prefill", ["mma", "tcgen05", "tcgen05x2"])
+@pytest.mark.parametrize("prefill", ["mma", "tcgen05"])
 def test_planner_counts_match_oracle_classification(index, prefill):
     bt = W.config(index, poison=False)
     d = Dev(bt)
@@ -59,10 +59,8 @@ def test_planner_counts_match_oracle_classification(index, prefill):
     finally:
         ops.set_decode_ctas(0)
         ops.set_prefill_kernel("auto")
-    # tcgen05 tiles stack the G q heads of a kv head: floor(128 / G) positions per tile; the
-    # two-tile items hold twice that
-    tiles = {"mma": 0, "tcgen05": 1, "tcgen05x2": 2}[prefill]
-    tile_q = tiles * (128 // (bt.num_q_heads // bt.num_kv_heads)) if tiles else 64
+    # tcgen05 tiles stack the G q heads of a kv head: floor(128 / G) positions per tile
+    tile_q = 128 // (bt.num_q_heads // bt.num_kv_heads) if prefill == "tcgen05" else 64
     assert header == _expected(bt, ctas, tile_q)
 
 
