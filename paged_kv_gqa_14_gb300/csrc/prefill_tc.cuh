@@ -18,7 +18,7 @@
 //              S from Q and K in shared memory (K-major), O from P in TMEM and V in shared
 //              memory (read as it lands, an MN-major operand), fp32 accumulators in TMEM,
 //              completion signalled with tcgen05.commit on mbarriers.
-//   warp 3     loads the V tiles the same way into their own 2-stage ring, so neither ring
+//   warp 3     loads the V tiles the same way into their own 3-stage ring, so neither ring
 //              waits for the other.
 //   warp 2     releases each V tile to the MMA, in an item's last tile after zeroing the rows
 //              of keys past the visible range (unloaded or past the context: 0 * NaN would
@@ -78,6 +78,24 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* m
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Two fp32 lanes per instruction (packed f32x2 FMA and add, Blackwell).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
 }
 
 // All 32 lanes wait; the outcome is made warp-uniform (any lane timing out aborts the warp).
@@ -383,16 +401,22 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
           resc = true;
         }
         const float base = m_run == NEG_INF ? 0.f : m_run;
-        // p = 2^(s * qscale - base): one FFMA and one ex2 per score; eight partial sums
-        float ls8[8];
+        // p = 2^(s * qscale - base): one ex2 per score, the FMA and the partial sums on packed
+        // f32x2 pairs (two scores per instruction), four pairs of partial sums
+        const float2 qs2 = make_float2(p.qscale, p.qscale);
+        const float2 nb2 = make_float2(-base, -base);
+        float2 ls4[4];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) ls8[x] = 0.f;
+        for (int x = 0; x < 4; ++x) ls4[x] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          sc[c] = fast_exp2(fmaf(sc[c], p.qscale, -base));
-          ls8[c & 7] += sc[c];
+        for (int c = 0; c < 128; c += 2) {
+          const float2 t = ffma2(make_float2(sc[c], sc[c + 1]), qs2, nb2);
+          sc[c] = fast_exp2(t.x);
+          sc[c + 1] = fast_exp2(t.y);
+          ls4[(c >> 1) & 3] = fadd2(ls4[(c >> 1) & 3], make_float2(sc[c], sc[c + 1]));
         }
-        const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+        const float2 ls2 = fadd2(fadd2(ls4[0], ls4[1]), fadd2(ls4[2], ls4[3]));
+        const float lsum = ls2.x + ls2.y;
         l_run = l_run * corr + lsum;
         if (jt > 0 && __any_sync(0xffffffffu, resc)) {
           // O is rescaled only once every P.V issued so far has landed in it
