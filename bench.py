@@ -428,7 +428,10 @@ def run_gpu(args, rank, world, local_rank):
     ops.set_kernel_events("plan")
     dec_ms = [a.elapsed_time(b) for a, b in dec]
     app_ms = [a.elapsed_time(b) for a, b in app]
-    pre_ms = [a.elapsed_time(b) for a, b in pre]
+    # the prefill kernel runs only when some span can hold two or more tokens (more tokens
+    # than sequences); otherwise its events are never recorded
+    has_prefill_kernel = bt.num_tokens > bt.num_seqs
+    pre_ms = [a.elapsed_time(b) for a, b in pre] if has_prefill_kernel else []
     att_ms = [a.elapsed_time(d[1]) for a, d in zip(att0, dec)]  # planner start .. decode end
     total_ms = replicas.max_over_ranks(total_ms, dist, device=dev)
     ms_step = total_ms / K
@@ -441,7 +444,7 @@ def run_gpu(args, rank, world, local_rank):
     # per SM over the share of the SMs the planner gave it (workspace header word 5)
     pf_flops = prefill_flops(bt)
     roofline_prefill = None
-    if pf_flops:
+    if pf_flops and pre_ms:
         pre_avg = sum(pre_ms) / K
         tpeak, tpeak_kind = bf16_peak()
         pf_tf = pf_flops / (pre_avg * 1e-3) / 1e12
@@ -595,7 +598,7 @@ def run_gpu(args, rank, world, local_rank):
             "kv_append": round(sum(app_ms) / K, 5),
             "paged_attention_call": round(sum(att_ms) / K, 5),
             "decode_splitk": round(dec_avg, 5),
-            "prefill_tiles": round(sum(pre_ms) / K, 5),
+            "prefill_tiles": round(sum(pre_ms) / K, 5) if pre_ms else None,
         },
         "kernels_ms_p10_p50_p90": {
             "kv_append": percentiles(app_ms),
@@ -631,7 +634,9 @@ def run_gpu(args, rank, world, local_rank):
                          "each step's result copied back on a second stream while the next step uploads and "
                          "runs (double-buffered out); the timed region ends with the last result on the host"),
         },
-        "gpu_launches": 4 * K,  # kv_append, planner, prefill tiles, decode split-K (+ merge)
+        # kv_append, planner, decode split-K (+ merge), and the prefill tiles when a span can
+        # hold two or more tokens
+        "gpu_launches": (4 if has_prefill_kernel else 3) * K,
         "clocks": clk,
         "decode_seqs": n_decode,
     }

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             int64_t max_ctx, int pps,
                                                             int decode_ctas, int tile_q, Plan plan,
                                                             int64_t max_tiles, SplitArgs split,
-                                                            unsigned int* err) {
+                                                            int rows_in_decode, unsigned int* err) {
   __shared__ int sm[3 * 32];
   __shared__ int carry[3];
   __shared__ unsigned long long pf_keytiles;  // 128-key tiles over all prefill q tiles (one kv head)
@@ -203,11 +203,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
           ok = false;
         }
       }
-      if (ok && span == 1) {
-        v.a = 1;
-        v.b = ceil_div(ceil_div(ctx, kPageTokens), pps);
+      if (ok && (span == 1 || (span > 1 && rows_in_decode))) {
+        // one decode entry per row: row r sees keys 0 .. ctx - span + r
+        v.a = span;
+        for (int r = 0; r < span; ++r) v.b += ceil_div(ceil_div(ctx - span + r + 1, kPageTokens), pps);
       }
-      if (ok && span > 1) {
+      if (ok && span > 1 && !rows_in_decode) {
         v.c = ceil_div(span, tile_q);
         if (split.on) {  // keys [0, kv_end) of q tile j are read in 128-key tiles
           unsigned long long sum = 0;
@@ -228,9 +229,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     ex.b += carry[1];
     ex.c += carry[2];
     if (v.a) {
-      plan.dec_seq[ex.a] = b;
-      plan.dec_count[ex.a] = 0;
-      plan.dec_unit[ex.a] = ex.b;
+      const int ctx = ctxl[b], s0 = qsl[b];
+      int unit = ex.b;
+      for (int r = 0; r < v.a; ++r) {
+        const int ctx_r = ctx - v.a + r + 1;
+        plan.dec_seq[ex.a + r] = b;
+        plan.dec_count[ex.a + r] = 0;
+        plan.dec_unit[ex.a + r] = unit;
+        plan.dec_ctx[ex.a + r] = ctx_r;
+        plan.dec_tq[ex.a + r] = s0 + r;
+        unit += ceil_div(ceil_div(ctx_r, kPageTokens), pps);
+      }
     }
     for (int j = 0; j < v.c; ++j) {
       if (ex.c + j < max_tiles) {
@@ -297,9 +306,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     if (i < n_dec) {
       plan.dec_slot[i] = ex.a + carry2;
       plan.dec_chunks[i] = v.a;
-      // the decode CTAs whose first unit c W falls in this sequence's units [u0, u1)
+      // the start records of the decode CTAs whose first unit c W falls in this entry's units
+      // [u0, u1)
       const int u0 = plan.dec_unit[i], u1 = plan.dec_unit[i + 1];
-      for (int c = ceil_div(u0, W); c * W < u1; ++c) plan.cta_first[c] = i;
+      const int4 r0 = make_int4(i, u0, u1, plan.dec_seq[i]);
+      const int4 r1 = make_int4(plan.dec_ctx[i], plan.dec_tq[i], 0, 0);
+      for (int c = ceil_div(u0, W); c * W < u1; ++c) {
+        plan.cta_rec[2 * c] = r0;
+        plan.cta_rec[2 * c + 1] = r1;
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) carry2 += tot.a;
@@ -444,10 +459,14 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   sp.dec_sm = kSplitDecodeSmBytesPerNs;
   sp.pf_sm = split_prefill_sm_bytes_per_ns(a.bs_log2);
   record_kernel_event(PKV_KERNEL_PLAN, false, stream);
+  // With no more tokens than sequences a prefill span is rare (it needs empty spans beside it):
+  // no prefill kernel is launched (its idle CTAs would hold the SMs between the planner and
+  // the decode), and the rows of such a span become decode entries.
+  const bool rows_in_decode = a.num_tokens <= a.num_seqs;
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
                              static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps,
                              a.decode_ctas, tile_q,
-                             a.plan, a.max_tiles, sp, a.err);
+                             a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.err);
   record_kernel_event(PKV_KERNEL_PLAN, true, stream);
   if (e != cudaSuccess) return e;
   auto prefill = [&](cudaStream_t s, bool pdl) -> cudaError_t {
@@ -470,8 +489,8 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
     return (a.head_dim == 128) ? launch_decode_g<128>(a, stream) : launch_decode_g<64>(a, stream);
   };
   if (!split) {
-    e = prefill(stream, true);
-    return e != cudaSuccess ? e : decode();
+    if (!rows_in_decode && (e = prefill(stream, true)) != cudaSuccess) return e;
+    return decode();
   }
   // fork after the planner, decode here, prefill on the side stream, join before returning
   std::lock_guard<std::mutex> hold(*static_cast<std::mutex*>(side.lock));
@@ -509,8 +528,12 @@ PlanSizes plan_sizes(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads, 
   off = align256(off + num_seqs * sizeof(int));
   s.off_dec_count = off;
   off = align256(off + num_seqs * sizeof(int));
-  s.off_cta_first = off;
-  off = align256(off + decode_ctas * sizeof(int));
+  s.off_dec_ctx = off;
+  off = align256(off + num_seqs * sizeof(int));
+  s.off_dec_tq = off;
+  off = align256(off + num_seqs * sizeof(int));
+  s.off_cta_rec = off;
+  off = align256(off + decode_ctas * 2 * sizeof(int4));
   s.off_pf_seq = off;
   off = align256(off + s.max_tiles * sizeof(int));
   s.off_pf_tile = off;
@@ -532,7 +555,9 @@ Plan plan_view(void* workspace, const PlanSizes& s) {
   p.dec_slot = reinterpret_cast<int*>(w + s.off_dec_slot);
   p.dec_chunks = reinterpret_cast<int*>(w + s.off_dec_chunks);
   p.dec_count = reinterpret_cast<int*>(w + s.off_dec_count);
-  p.cta_first = reinterpret_cast<int*>(w + s.off_cta_first);
+  p.dec_ctx = reinterpret_cast<int*>(w + s.off_dec_ctx);
+  p.dec_tq = reinterpret_cast<int*>(w + s.off_dec_tq);
+  p.cta_rec = reinterpret_cast<int4*>(w + s.off_cta_rec);
   p.pf_seq = reinterpret_cast<int*>(w + s.off_pf_seq);
   p.pf_tile = reinterpret_cast<int*>(w + s.off_pf_tile);
   p.part_ml = reinterpret_cast<float*>(w + s.off_part_ml);

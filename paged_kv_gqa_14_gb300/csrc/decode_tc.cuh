@@ -137,9 +137,12 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   const int* hdr = p.plan.header;
   const int U = hdr[1];
   const int W = hdr[2];
-  // the decode sequence holding this CTA's first unit, from the planner (read alongside the
-  // header; meaningless, and unused, for a CTA without units)
-  const int i_first = p.plan.cta_first[blockIdx.x];
+  // this CTA's start record from the planner, read alongside the header: the decode entry
+  // holding its first unit, that entry's unit range, sequence, context and query row
+  // (meaningless, and unused, for a CTA without units)
+  const int4 rec0 = p.plan.cta_rec[2 * blockIdx.x];
+  const int4 rec1 = p.plan.cta_rec[2 * blockIdx.x + 1];
+  const int i_first = rec0.x;
   const int ubeg = blockIdx.x * W;
   const int uend = min(U, ubeg + W);
   if (ubeg >= uend) return;  // CTA-uniform
@@ -169,9 +172,9 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     const int bhalf = rem - bp * HALVES;
     const bool lane_has_box = lane < 2 * per_kv;
     int i = i_first;
-    int ustart = dec_unit[i], unext = dec_unit[i + 1];
-    int b = p.plan.dec_seq[i];
-    int ctx = p.context_lens[b];
+    int ustart = rec0.y, unext = rec0.z;
+    int b = rec0.w;
+    int ctx = rec1.x;
     int npages = ceil_div(ctx, 16);
     // page gp: block gp >> s4 and its rows from (16 gp) & bmask when blocks hold 16 << s4
     // tokens; blocks 2 gp and 2 gp + 1 (the second only if it holds context) when they hold 8
@@ -186,7 +189,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
         ustart = unext;
         unext = dec_unit[i + 1];
         b = p.plan.dec_seq[i];
-        ctx = p.context_lens[b];
+        ctx = p.plan.dec_ctx[i];
         npages = ceil_div(ctx, 16);
       }
       const int pg0 = (u - ustart) * pps;
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   float acc[KS][4];    // O^T: dims 16mt + gr (+8), heads 2tig (+1)
   float mrun[2], lrun[2];
   int i = i_first;
-  int ustart = 0, unext = 0, b = 0, ctx = 0, npages = 0;
+  int ustart = 0, unext = 0, ctx = 0, npages = 0;
   int64_t tq = 0;
   bool seg_start = true;
   bool ok = true;
@@ -245,12 +248,18 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   const uint32_t stage_base = smem_u32(stages);
   for (int u = ubeg; u < uend; ++u, ++it) {
     if (seg_start) {
-      ustart = dec_unit[i];
-      unext = dec_unit[i + 1];
-      b = p.plan.dec_seq[i];
-      ctx = p.context_lens[b];
+      if (i == i_first) {
+        ustart = rec0.y;
+        unext = rec0.z;
+        ctx = rec1.x;
+        tq = rec1.y;
+      } else {
+        ustart = dec_unit[i];
+        unext = dec_unit[i + 1];
+        ctx = p.plan.dec_ctx[i];
+        tq = p.plan.dec_tq[i];
+      }
       npages = ceil_div(ctx, 16);
-      tq = p.qsl[b];
       const bool hv = gr < G;
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
           p.q + tq * p.q_st + static_cast<int64_t>(h * G + (hv ? gr : 0)) * p.q_sh);

@@ -35,7 +35,8 @@ constexpr int kTensorDecodeMinGroup = 1;
 // The planner kernel fills these arrays in the caller's workspace; the decode, prefill
 // and merge kernels read them.  All offsets are 256-byte aligned.
 //
-// header[0] number of decode sequences (span == 1)            n_dec
+// header[0] number of decode entries (spans of one row; with no prefill kernel, also one entry
+//           per row of a longer span)                           n_dec
 // header[1] total decode work units                            U
 // header[2] work units per decode CTA                          W = ceil(U / C)
 // header[3] number of prefill (seq, q-tile) work items         n_tiles
@@ -52,8 +53,12 @@ struct Plan {
   int* dec_slot;    // [B]      first partial slot of each decode sequence
   int* dec_chunks;  // [B]      number of decode CTAs that touch the sequence
   int* dec_count;   // [B]      split states written so far (zeroed by the planner)
-  int* cta_first;   // [C]      decode CTA c: index in the decode list of the sequence holding
-                    //          its first unit c W (written only for CTAs that have units)
+  int* dec_ctx;     // [B]      keys the entry's query row sees (its context, or for a prefill
+                    //          row computed by the decode path, ctx - n + r + 1)
+  int* dec_tq;      // [B]      the entry's query row (token index)
+  int4* cta_rec;    // [C][2]   decode CTA c's start record: {entry i holding its first unit c W,
+                    //          dec_unit[i], dec_unit[i + 1], sequence}, {context, query row, 0, 0}
+                    //          (written only for CTAs that have units)
   int* pf_seq;      // [max_tiles]  prefill work item: sequence id
   int* pf_tile;     // [max_tiles]  prefill work item: q-tile index within the span
   float* part_ml;   // [S_max][Hq][2]   split state: running max (log2 domain), sum of weights
@@ -63,7 +68,8 @@ struct Plan {
 struct PlanSizes {
   int64_t num_seqs, num_tokens, num_q_heads, head_dim, decode_ctas;
   int64_t max_tiles, max_slots;
-  size_t off_header, off_dec_seq, off_dec_unit, off_dec_slot, off_dec_chunks, off_dec_count, off_cta_first;
+  size_t off_header, off_dec_seq, off_dec_unit, off_dec_slot, off_dec_chunks, off_dec_count, off_dec_ctx,
+      off_dec_tq, off_cta_rec;
   size_t off_pf_seq, off_pf_tile, off_part_ml, off_part_acc, total;
 };
 

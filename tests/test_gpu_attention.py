@@ -421,3 +421,30 @@ def test_bounded_wait_runs_out_and_reports_timeout():
     torch.cuda.synchronize()
     assert ops.get_device_error() == 0
     assert_close(got, ref, "after a timed-out call")
+
+
+@pytest.mark.parametrize("decode_kernel", ["simt", "tensor"], indirect=True)
+@pytest.mark.parametrize("case", [
+    ([40, 300, 17, 64], [0, 3, 0, 1]),   # as many tokens as sequences: a 3-row span beside empty ones
+    ([50, 129, 33], [2, 0, 0]),          # fewer tokens than sequences
+    ([2000, 5], [2, 0]),                 # a long context
+])
+def test_prefill_rows_without_more_tokens_than_sequences(case, decode_kernel):
+    # num_tokens <= num_seqs: no prefill kernel is launched; the planner turns each row of a
+    # longer span into a decode entry that sees its own causal context (keys 0 .. ctx - n + r)
+    ctx, spans = case
+    pages = sum(-(-c // 16) for c in ctx)
+    bt = W.make_batch(ctx, spans, 16, 8, 128, pages + 4, seed=sum(ctx))
+    assert bt.num_tokens <= bt.num_seqs
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache,
+                                     bt.v_cache, bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    got, d = _attend_oracle_inputs(bt, q_rot, kc, vc)
+    assert_close(got, ref, f"rows in the decode path, {case}, decode={decode_kernel}")
+    # the plan: one decode entry per row, no prefill work entries
+    ws = ops.alloc_workspace(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
+                             bt.block_tables.shape[1])
+    ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale, workspace=ws)
+    torch.cuda.synchronize()
+    header = ws[:16].cpu().numpy().view(np.int32)[:4].tolist()
+    assert header[0] == sum(spans) and header[3] == 0
