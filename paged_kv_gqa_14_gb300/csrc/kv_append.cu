@@ -3,14 +3,16 @@
 // "Week 4 -- Paged KV cache": pool of fixed-size blocks addressed by slot; the block size is
 // 16 by default and any power of two from 8 to 128 here).
 //
-// One CTA per new token.  Its q, k and v rows are read first (their addresses do not
-// depend on the position), then the d/2 rotation angles are computed once into shared
-// memory: angle = pos * f_i with f_i = theta^(-2i/d) (fp64 on the host), taken modulo one
-// turn exactly in 64-bit integer arithmetic (RopeFreqs), split exactly into a quarter turn
+// One warp per new token, four tokens per CTA, no CTA-wide barrier.  A warp first issues the
+// loads of its token's q, k and v rows (their addresses do not depend on the position) and of
+// its position and slot, then computes the d/2 rotation angles into a warp-private table in
+// shared memory: angle = pos * f_i with f_i = theta^(-2i/d) (fp64 on the host), taken modulo
+// one turn exactly in 64-bit integer arithmetic (RopeFreqs), split exactly into a quarter turn
 // and a remainder in [-pi/4, pi/4) that reaches fp32 with one rounding, then sincosf in fp32
 // and an exact quarter-turn swap.  Every head of q (in place) and k (into the slot) is
 // rotated pairwise (i, i + d/2) in fp32 and rounded to bf16 nearest-even; v is a 16-byte
-// vector copy.  All global accesses are 16-byte vectors along head_dim.
+// vector copy.  All global accesses are 16-byte vectors along head_dim; the lanes of a warp
+// cover consecutive 16-byte chunks of a head row, so every access is coalesced.
 //
 // Error of a rotated fp32 value before its bf16 rounding, for a pair (x, y) at a position
 // below 2^31: the fp32 remainder angle is within 2^-25 rad of the exact one (one rounding at
@@ -27,12 +29,11 @@
 namespace pkv {
 namespace {
 
-// Threads per token: four warps, or two when the step has more tokens than one wave of
-// four-warp CTAs holds (8 CTAs of 128 threads per SM at 64 registers): 16 two-warp CTAs fit on
-// an SM, so the mixed chunked-prefill step's 2248 tokens run in one wave on 152 SMs.  Measured
-// on GB300: two warps take the 2248-token append from 12.6 to 11.6 us but make the 256-token
-// decode step 2 us slower (eager), so the choice follows the token count.
-constexpr int kAppendWaveCtas = 8;  // four-warp CTAs resident per SM
+constexpr int kAppendWarps = 4;  // warps per CTA
+// Warps per token (each computes the whole angle table, so they never synchronise).  Measured
+// on GB300 on the 2248-token mixed step: one warp 10.5 us, two warps 10.5-10.9 us, one CTA of
+// two warps per token with a CTA barrier 10.8 us.
+constexpr int kWarpsPerToken = 1;
 
 // Where each token's position and slot come from: explicit arrays, or (qsl != nullptr)
 // derived on the device from the scheduler's tables.
@@ -88,7 +89,8 @@ __device__ __forceinline__ float2 cos_sin_of_turn(unsigned long long turn) {
   }
 }
 
-__device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float2* cs) {
+template <typename CS>
+__device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const CS& cs) {
   uint32_t* a = reinterpret_cast<uint32_t*>(&lo);
   uint32_t* b = reinterpret_cast<uint32_t*>(&hi);
 #pragma unroll
@@ -105,7 +107,7 @@ __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float2* cs) 
 // token's sequence b is the last one with query_start_loc[b] <= t (found by a warp-wide
 // search, 32 samples per round), it sits at position ctx_b - n_b + (t - qsl[b]) and its slot
 // is row pos % bs of block block_tables[b][pos / bs].  Tokens outside every span get slot -1.
-__device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t num_blocks, unsigned int* err,
+__device__ __forceinline__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t num_blocks, unsigned int* err,
                             int64_t& pos, int64_t& slot) {
   const int32_t* qsl = src.qsl;
   int lo = 0, hi = static_cast<int>(src.num_seqs);  // inclusive range of qsl indices
@@ -152,39 +154,54 @@ __device__ void derive_slot(const AppendSrc& src, int64_t t, int lane, int64_t n
   slot = (static_cast<int64_t>(blk) << src.bs_log2) + (pos & ((int64_t(1) << src.bs_log2) - 1));
 }
 
-// Row items a thread holds in registers from the start (item = one 16-byte chunk pair of a q
-// or k head, or one 16-byte chunk of a v head; items past these counts are read later).
-constexpr int kQPrefetch = 2;  // q chunk pairs per thread: Hq * d / 16 <= 2 x threads
+// Row items a lane holds in registers from the start (a q or k item is one 16-byte chunk pair
+// (i, i + d/2) of a head, a v item one 16-byte chunk); items past these counts are read later.
+constexpr int kQPrefetch = 4 / kWarpsPerToken;  // q items per lane: 16 q heads at d 128 have 128
+constexpr int kKPrefetch = 2 / kWarpsPerToken;  // k items per lane: 8 kv heads at d 128 have 64
+constexpr int kVPrefetch = 4 / kWarpsPerToken;  // v items per lane: 8 kv heads at d 128 have 128
 
-template <int D, int kAppendThreads>
-__global__ void __launch_bounds__(kAppendThreads, kAppendThreads == 64 ? 16 : kAppendWaveCtas) kv_append_kernel(
+template <int D>
+__global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(
     bf16* __restrict__ q, int64_t q_st, int64_t q_sh, const bf16* __restrict__ k, int64_t k_st,
     int64_t k_sh, const bf16* __restrict__ v, int64_t v_st, int64_t v_sh, const __grid_constant__ AppendSrc src,
-    bf16* __restrict__ k_cache, bf16* __restrict__ v_cache, int64_t num_slots, int hq, int hkv,
+    bf16* __restrict__ k_cache, bf16* __restrict__ v_cache, int64_t num_tokens, int64_t num_slots, int hq, int hkv,
     const __grid_constant__ RopeFreqs fr, unsigned int* err) {
   constexpr int HALF = D / 2;
   constexpr int CH = HALF / 8;  // 16-byte chunks per half head
   constexpr int VCH = D / 8;    // 16-byte chunks per v head
-  constexpr int kVPrefetch = 128 / kAppendThreads;  // v chunks per thread: Hkv * d / 8 <= 128
-  __shared__ float2 cs[HALF];
-  __shared__ int64_t s_pos, s_slot;
+  __shared__ float2 cs_all[kAppendWarps][HALF];
 
   pdl_wait();  // q, k, v and the index inputs may come from the previous kernel
   pdl_trigger();
-  const int64_t t = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kTokensPerCta = kAppendWarps / kWarpsPerToken;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kTokensPerCta + warp / kWarpsPerToken;
+  const int sub = warp % kWarpsPerToken;  // this warp takes items sub, sub + W, ... (W = warps per token)
+  constexpr int kStride = 32 * kWarpsPerToken;
+  if (t >= num_tokens) return;  // warp-uniform; nothing below synchronises more than the warp
+  float2* cs = cs_all[warp];
   const int nq = hq * CH, nk = hkv * CH, nv = hkv * VCH;
   auto q_row = [&](int item, int& c) -> bf16* {
     const int head = item / CH;
     c = item - head * CH;
     return q + t * q_st + head * q_sh;
   };
-  // The token's rows do not depend on its position or slot: they are read first, so their
-  // latency overlaps the index reads and the angle computation.
-  uint4 qlo[kQPrefetch], qhi[kQPrefetch];
+  auto k_row = [&](int item, int& c) -> const bf16* {
+    const int head = item / CH;
+    c = item - head * CH;
+    return k + t * k_st + head * k_sh;
+  };
+  // position and slot first (explicit arrays: one load each, lane 0)
+  int64_t pos = 0, slot = -1;
+  if (!src.qsl && lane == 0) {
+    pos = src.positions[t];
+    slot = src.slots[t];
+  }
+  // the token's rows
+  uint4 qlo[kQPrefetch], qhi[kQPrefetch], klo[kKPrefetch], khi[kKPrefetch], vx[kVPrefetch];
 #pragma unroll
   for (int j = 0; j < kQPrefetch; ++j) {
-    const int item = tid + j * kAppendThreads;
+    const int item = lane + 32 * sub + kStride * j;
     if (item < nq) {
       int c;
       const bf16* row = q_row(item, c);
@@ -192,95 +209,101 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendThreads == 64 ? 16 : kA
       qhi[j] = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
     }
   }
-  uint4 klo = make_uint4(0u, 0u, 0u, 0u), khi = klo, vx[kVPrefetch];
-  if (tid < nk) {
-    const int h = tid / CH, c = tid - (tid / CH) * CH;
-    const bf16* row = k + t * k_st + h * k_sh;
-    klo = *reinterpret_cast<const uint4*>(row + c * 8);
-    khi = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
+#pragma unroll
+  for (int j = 0; j < kKPrefetch; ++j) {
+    const int item = lane + 32 * sub + kStride * j;
+    if (item < nk) {
+      int c;
+      const bf16* row = k_row(item, c);
+      klo[j] = *reinterpret_cast<const uint4*>(row + c * 8);
+      khi[j] = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
+    }
   }
 #pragma unroll
   for (int j = 0; j < kVPrefetch; ++j) {
-    const int item = tid + j * kAppendThreads;
-    vx[j] = make_uint4(0u, 0u, 0u, 0u);
+    const int item = lane + 32 * sub + kStride * j;
     if (item < nv) {
       const int h = item / VCH, c = item - (item / VCH) * VCH;
       vx[j] = *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8);
     }
   }
-
-  if (tid < 32) {
-    int64_t p_, s_;
-    if (src.qsl) {
-      derive_slot(src, t, tid, num_slots >> src.bs_log2, err, p_, s_);
-    } else {
-      p_ = src.positions[t];
-      s_ = src.slots[t];
-    }
-    if (tid == 0) {
-      s_pos = p_;
-      s_slot = s_;
-      if (src.pos_out) src.pos_out[t] = p_;
-      if (src.slot_out) src.slot_out[t] = s_;
-    }
+  if (src.qsl) {
+    derive_slot(src, t, lane, num_slots >> src.bs_log2, err, pos, slot);
+  } else {
+    pos = __shfl_sync(0xffffffffu, pos, 0);
+    slot = __shfl_sync(0xffffffffu, slot, 0);
   }
-  __syncthreads();
-  const int64_t pos = s_pos;
-  const int64_t slot = s_slot;
+  if (lane == 0 && sub == 0) {
+    if (src.pos_out) src.pos_out[t] = pos;
+    if (src.slot_out) src.slot_out[t] = slot;
+  }
 
   // the token's angles modulo one turn: pos F_i mod 2^64 in 0.64 fixed point
-  for (int i = tid; i < HALF; i += kAppendThreads)
-    cs[i] = cos_sin_of_turn(static_cast<unsigned long long>(pos) * fr.F[i]);
+  for (int i = lane; i < HALF; i += 32) cs[i] = cos_sin_of_turn(static_cast<unsigned long long>(pos) * fr.F[i]);
   const bool in_range = slot < num_slots;
   const bool write_kv = slot >= 0 && in_range;
-  if (!in_range && tid == 0) raise_error(err, PKV_DEVERR_SLOT_RANGE);
-  __syncthreads();
+  if (!in_range && lane == 0 && sub == 0) raise_error(err, PKV_DEVERR_SLOT_RANGE);
+  __syncwarp();
+  // every item of this lane is chunk c = lane % CH of some head (32 is a multiple of CH): its
+  // eight (cos, sin) pairs are held in registers
+  float2 my_cs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) my_cs[i] = cs[(lane % CH) * 8 + i];
 
   // q heads rotated in place
 #pragma unroll
   for (int j = 0; j < kQPrefetch; ++j) {
-    const int item = tid + j * kAppendThreads;
+    const int item = lane + 32 * sub + kStride * j;
     if (item < nq) {
       int c;
       bf16* row = q_row(item, c);
-      rotate8(qlo[j], qhi[j], cs + c * 8);
+      rotate8(qlo[j], qhi[j], my_cs);
       *reinterpret_cast<uint4*>(row + c * 8) = qlo[j];
       *reinterpret_cast<uint4*>(row + HALF + c * 8) = qhi[j];
     }
   }
-  for (int item = tid + kQPrefetch * kAppendThreads; item < nq; item += kAppendThreads) {
+  for (int item = lane + 32 * sub + kStride * kQPrefetch; item < nq; item += kStride) {
     int c;
     bf16* row = q_row(item, c);
     uint4 lo = *reinterpret_cast<const uint4*>(row + c * 8);
     uint4 hi = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
-    rotate8(lo, hi, cs + c * 8);
+    rotate8(lo, hi, my_cs);
     *reinterpret_cast<uint4*>(row + c * 8) = lo;
     *reinterpret_cast<uint4*>(row + HALF + c * 8) = hi;
   }
   if (!write_kv) return;
   // k heads rotated into the cache row of `slot`, v heads copied there
-  for (int item = tid; item < nk; item += kAppendThreads) {
-    const int h = item / CH, c = item - (item / CH) * CH;
-    uint4 lo = klo, hi = khi;
-    if (item >= kAppendThreads) {
-      const bf16* row = k + t * k_st + h * k_sh;
-      lo = *reinterpret_cast<const uint4*>(row + c * 8);
-      hi = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
+#pragma unroll
+  for (int j = 0; j < kKPrefetch; ++j) {
+    const int item = lane + 32 * sub + kStride * j;
+    if (item < nk) {
+      const int h = item / CH, c = item - (item / CH) * CH;
+      rotate8(klo[j], khi[j], my_cs);
+      bf16* dst = k_cache + (slot * hkv + h) * D;
+      *reinterpret_cast<uint4*>(dst + c * 8) = klo[j];
+      *reinterpret_cast<uint4*>(dst + HALF + c * 8) = khi[j];
     }
-    rotate8(lo, hi, cs + c * 8);
+  }
+  for (int item = lane + 32 * sub + kStride * kKPrefetch; item < nk; item += kStride) {
+    int c;
+    const bf16* row = k_row(item, c);
+    const int h = item / CH;
+    uint4 lo = *reinterpret_cast<const uint4*>(row + c * 8);
+    uint4 hi = *reinterpret_cast<const uint4*>(row + HALF + c * 8);
+    rotate8(lo, hi, my_cs);
     bf16* dst = k_cache + (slot * hkv + h) * D;
     *reinterpret_cast<uint4*>(dst + c * 8) = lo;
     *reinterpret_cast<uint4*>(dst + HALF + c * 8) = hi;
   }
 #pragma unroll
   for (int j = 0; j < kVPrefetch; ++j) {
-    const int item = tid + j * kAppendThreads;
+    const int item = lane + 32 * sub + kStride * j;
     if (item < nv) {
       const int h = item / VCH, c = item - (item / VCH) * VCH;
       *reinterpret_cast<uint4*>(v_cache + (slot * hkv + h) * D + c * 8) = vx[j];
     }
   }
-  for (int item = tid + kVPrefetch * kAppendThreads; item < nv; item += kAppendThreads) {
+  for (int item = lane + 32 * sub + kStride * kVPrefetch; item < nv; item += kStride) {
     const int h = item / VCH, c = item - (item / VCH) * VCH;
     *reinterpret_cast<uint4*>(v_cache + (slot * hkv + h) * D + c * 8) =
         *reinterpret_cast<const uint4*>(v + t * v_st + h * v_sh + c * 8);
@@ -339,8 +362,8 @@ const RopeFreqs& rope_freqs(double theta, int head_dim) {
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
   const RopeFreqs& fr = rope_freqs(a.theta, a.head_dim);
-  const dim3 grid(static_cast<unsigned>(a.num_tokens));
-  const bool two_warps = a.num_tokens > static_cast<int64_t>(kAppendWaveCtas) * device_sm_count();
+  constexpr int kTokensPerCta = kAppendWarps / kWarpsPerToken;
+  const dim3 grid(static_cast<unsigned>((a.num_tokens + kTokensPerCta - 1) / kTokensPerCta));
   AppendSrc src;
   src.positions = a.positions;
   src.slots = a.slots;
@@ -354,13 +377,12 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   src.pos_out = a.positions_out;
   src.slot_out = a.slots_out;
   record_kernel_event(PKV_KERNEL_APPEND, false, stream);
-  auto* kernel = a.head_dim == 128 ? (two_warps ? kv_append_kernel<128, 64> : kv_append_kernel<128, 128>)
-                                   : (two_warps ? kv_append_kernel<64, 64> : kv_append_kernel<64, 128>);
+  auto* kernel = a.head_dim == 128 ? kv_append_kernel<128> : kv_append_kernel<64>;
   const cudaError_t e = launch_pdl(
-      kernel, grid, dim3(two_warps ? 64 : 128), 0, stream,
+      kernel, grid, dim3(kAppendWarps * 32), 0, stream,
       static_cast<bf16*>(a.q), a.q_st, a.q_sh, static_cast<const bf16*>(a.k), a.k_st, a.k_sh,
       static_cast<const bf16*>(a.v), a.v_st, a.v_sh, src, static_cast<bf16*>(a.k_cache),
-      static_cast<bf16*>(a.v_cache), a.num_slots, a.hq, a.hkv, fr, a.err);
+      static_cast<bf16*>(a.v_cache), a.num_tokens, a.num_slots, a.hq, a.hkv, fr, a.err);
   record_kernel_event(PKV_KERNEL_APPEND, true, stream);
   return e;
 }
