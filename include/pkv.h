@@ -202,9 +202,15 @@ PKV_API size_t pkv_paged_attention_workspace_size(int64_t num_tokens, int64_t nu
  *            num_q_heads / num_kv_heads in [1, 8].
  * Ordering: all work is ordered after earlier work on `stream`, and later work on `stream`
  * is ordered after all of it.  With prefill spans (num_tokens > num_seqs) the prefill tiles
- * may run on a second stream of the library's own, forked from `stream` after the planner
- * and joined back into it before the call returns (pkv_set_overlap); this also holds
- * inside a CUDA graph capture of `stream`.
+ * may run on a second stream, forked from `stream` after the planner and joined back into it
+ * before the call returns (pkv_set_overlap): the caller's own (pkv_paged_attention_ex) or the
+ * library's, one per device, shared by all callers.  The library's second stream is used
+ * only when no CUDA graph capture holds it, or when the capture holding it is the one this
+ * call is captured into; otherwise the call runs its kernels in the serial order on `stream`
+ * (same results up to fp32 rounding of the decode rows).  So a capture of `stream` and
+ * eager calls on other streams can be open at the same time.  With num_tokens <= num_seqs
+ * no prefill kernel is launched: the rows of a longer span (which then needs empty spans
+ * beside it) are computed by the decode path, each row over its own causal context.
  */
 PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64_t q_stride_head,
                         const void* k_cache_dev, const void* v_cache_dev,
@@ -217,6 +223,57 @@ PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64
                         int64_t num_tokens, int64_t num_q_heads, int64_t num_kv_heads,
                         int64_t head_dim, float scale,
                         void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_attention_options -- per-call settings of pkv_paged_attention_ex.  Zero-initialise,
+ * set struct_size = sizeof(pkv_attention_options), then set what the call needs; a zero field
+ * keeps the process default (the pkv_set_* functions below).
+ *   decode_kernel   0 default, 1 CUDA cores, 2 tensor cores (as pkv_set_decode_kernel)
+ *   prefill_kernel  0 default, 1 mma.sync tiles, 2 tcgen05 tiles (as pkv_set_prefill_kernel)
+ *   overlap         0 default, 1 prefill tiles beside the decode when possible, 2 serial order
+ *   decode_ctas     0 default, else the decode grid of this call (1 .. 65536); the workspace
+ *                   must then hold pkv_paged_attention_workspace_size_ex(..., decode_ctas)
+ *   side_stream, fork_event, join_event
+ *                   all NULL: the library's own second stream for the prefill beside the
+ *                   decode; else a caller-owned stream (cudaStream_t) and two caller-created
+ *                   events (cudaEvent_t, timing disabled) that order it after the planner and
+ *                   back into `stream` -- independent callers on different streams then never
+ *                   share, or serialise on, a stream of the library's.  The caller must not
+ *                   use them for anything else until the call's work has completed.
+ * Invalid values give PKV_ERR_SHAPE; one or two of the three handles given give PKV_ERR_NULL.
+ */
+typedef struct pkv_attention_options {
+  uint32_t struct_size;
+  int32_t decode_kernel;
+  int32_t prefill_kernel;
+  int32_t overlap;
+  int32_t decode_ctas;
+  int32_t reserved;  /* 0 */
+  void* side_stream;
+  void* fork_event;
+  void* join_event;
+} pkv_attention_options;
+
+/* pkv_paged_attention with per-call settings (NULL options: the same as pkv_paged_attention). */
+PKV_API int pkv_paged_attention_ex(const void* q_dev, int64_t q_stride_token, int64_t q_stride_head,
+                                   const void* k_cache_dev, const void* v_cache_dev,
+                                   int64_t num_blocks, int64_t block_size,
+                                   const int32_t* block_tables_dev, int64_t block_tables_stride,
+                                   int64_t max_blocks_per_seq,
+                                   const int32_t* context_lens_dev, const int32_t* query_start_loc_dev,
+                                   int64_t num_seqs,
+                                   void* out_dev, int64_t out_stride_token, int64_t out_stride_head,
+                                   int64_t num_tokens, int64_t num_q_heads, int64_t num_kv_heads,
+                                   int64_t head_dim, float scale,
+                                   void* workspace_dev, size_t workspace_bytes, void* stream,
+                                   const pkv_attention_options* options);
+
+/* Workspace bytes for a call with options.decode_ctas = decode_ctas (0: the process default,
+ * as pkv_paged_attention_workspace_size).  Returns 0 for invalid sizes. */
+PKV_API size_t pkv_paged_attention_workspace_size_ex(int64_t num_tokens, int64_t num_seqs,
+                                                     int64_t num_q_heads, int64_t num_kv_heads,
+                                                     int64_t head_dim, int64_t max_blocks_per_seq,
+                                                     int32_t decode_ctas);
 
 /*
  * pkv_paged_attention_noalloc -- pkv_paged_attention for callers that cannot allocate
@@ -253,8 +310,12 @@ PKV_API int pkv_paged_attention_noalloc(const void* q_dev, int64_t q_stride_toke
                                         int64_t head_dim, float scale, void* stream);
 
 /*
+ * The pkv_set_* settings below are process-wide defaults for calls without options (every
+ * thread and stream of the process sees a change at once); they are meant for tests and
+ * tuning.  Per-call settings: pkv_paged_attention_ex.
+ *
  * pkv_set_decode_ctas -- override the number of CTAs the decode split-K kernel uses
- * (0 = automatic: one per SM).  Process-wide; meant for tests and tuning.  Changes the
+ * (0 = automatic: one per SM; at most 65536).  Changes the
  * split points, hence rounding, never the result beyond fp32 rounding.  Returns PKV_OK,
  * or PKV_ERR_SHAPE for a negative value.
  */

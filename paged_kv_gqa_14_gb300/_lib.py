@@ -36,6 +36,13 @@ SIGNATURES = {
          _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_float, _c_p, ctypes.c_size_t,
          _c_p],
     ),
+    "pkv_paged_attention_ex": (
+        ctypes.c_int,
+        [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i64,
+         _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_float, _c_p, ctypes.c_size_t,
+         _c_p, _c_p],
+    ),
+    "pkv_paged_attention_workspace_size_ex": (ctypes.c_size_t, [_c_i64] * 6 + [ctypes.c_int32]),
     "pkv_paged_attention_noalloc": (
         ctypes.c_int,
         [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i64,
@@ -73,6 +80,16 @@ DEVERR = {
 KERNELS = {"kv_append": 1, "plan": 2, "prefill": 3, "decode": 4}
 
 _lib = None
+
+
+class AttentionOptions(ctypes.Structure):
+    """pkv_attention_options (include/pkv.h)."""
+
+    _fields_ = [("struct_size", ctypes.c_uint32), ("decode_kernel", ctypes.c_int32),
+                ("prefill_kernel", ctypes.c_int32), ("overlap", ctypes.c_int32),
+                ("decode_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("side_stream", ctypes.c_void_p), ("fork_event", ctypes.c_void_p),
+                ("join_event", ctypes.c_void_p)]
 
 
 class PkvError(RuntimeError):

@@ -16,6 +16,7 @@ static __device__ unsigned int g_error_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxDecodeCtas = 1 << 16;  // largest decode grid a call may ask for
 std::once_flag g_dev_once[kMaxDevices];
 unsigned int* g_err_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
@@ -147,7 +148,7 @@ int pkv_set_fault_injection(int kind) {
 }
 
 int pkv_set_decode_ctas(int32_t ctas) {
-  if (ctas < 0) return PKV_ERR_SHAPE;
+  if (ctas < 0 || ctas > kMaxDecodeCtas) return PKV_ERR_SHAPE;
   g_decode_ctas_override.store(ctas);
   return PKV_OK;
 }
@@ -289,24 +290,43 @@ int pkv_rope_turn_table(double rope_theta, int64_t head_dim, uint64_t* out) {
   return PKV_OK;
 }
 
-size_t pkv_paged_attention_workspace_size(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads,
-                                          int64_t num_kv_heads, int64_t head_dim,
-                                          int64_t max_blocks_per_seq) {
+size_t pkv_paged_attention_workspace_size_ex(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads,
+                                             int64_t num_kv_heads, int64_t head_dim, int64_t max_blocks_per_seq,
+                                             int32_t decode_ctas) {
   if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq < 0)
     return 0;
   if (head_dim != 64 && head_dim != 128) return 0;
-  const int ctas = decode_ctas_for_device();
+  if (decode_ctas < 0 || decode_ctas > kMaxDecodeCtas) return 0;
+  const int ctas = decode_ctas > 0 ? decode_ctas : decode_ctas_for_device();
   if (ctas <= 0) return 0;
   return plan_sizes(num_tokens, num_seqs, num_q_heads, head_dim, ctas).total;
 }
 
-int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k_cache,
-                        const void* v_cache, int64_t num_blocks, int64_t block_size,
-                        const int32_t* block_tables, int64_t bt_stride, int64_t max_blocks_per_seq,
-                        const int32_t* context_lens, const int32_t* query_start_loc, int64_t num_seqs,
-                        void* out, int64_t o_st, int64_t o_sh, int64_t num_tokens, int64_t num_q_heads,
-                        int64_t num_kv_heads, int64_t head_dim, float scale, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+size_t pkv_paged_attention_workspace_size(int64_t num_tokens, int64_t num_seqs, int64_t num_q_heads,
+                                          int64_t num_kv_heads, int64_t head_dim,
+                                          int64_t max_blocks_per_seq) {
+  return pkv_paged_attention_workspace_size_ex(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                               max_blocks_per_seq, 0);
+}
+
+}  // extern "C"
+
+namespace {
+
+int paged_attention_impl(const void* q, int64_t q_st, int64_t q_sh, const void* k_cache, const void* v_cache,
+                         int64_t num_blocks, int64_t block_size, const int32_t* block_tables, int64_t bt_stride,
+                         int64_t max_blocks_per_seq, const int32_t* context_lens, const int32_t* query_start_loc,
+                         int64_t num_seqs, void* out, int64_t o_st, int64_t o_sh, int64_t num_tokens,
+                         int64_t num_q_heads, int64_t num_kv_heads, int64_t head_dim, float scale, void* workspace,
+                         size_t workspace_bytes, void* stream, const pkv_attention_options* opt) {
+  if (opt) {
+    if (opt->struct_size != sizeof(pkv_attention_options)) return PKV_ERR_SHAPE;
+    if (opt->decode_kernel < 0 || opt->decode_kernel > 2 || opt->prefill_kernel < 0 || opt->prefill_kernel > 2 ||
+        opt->overlap < 0 || opt->overlap > 2 || opt->decode_ctas < 0 || opt->decode_ctas > kMaxDecodeCtas)
+      return PKV_ERR_SHAPE;
+    const int given = (opt->side_stream != nullptr) + (opt->fork_event != nullptr) + (opt->join_event != nullptr);
+    if (given != 0 && given != 3) return PKV_ERR_NULL;
+  }
   if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
       max_blocks_per_seq < 0)
     return PKV_ERR_SHAPE;
@@ -329,7 +349,7 @@ int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k
   if ((q_st | q_sh | o_st | o_sh) & 7) return PKV_ERR_ALIGN;
   const int dev = current_device();
   if (!device_setup(dev)) return PKV_ERR_CUDA;
-  const int ctas = decode_ctas_for_device();
+  const int ctas = (opt && opt->decode_ctas > 0) ? opt->decode_ctas : decode_ctas_for_device();
   const PlanSizes ps = plan_sizes(num_tokens, num_seqs, num_q_heads, head_dim, ctas);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < ps.total)
     return PKV_ERR_WORKSPACE;
@@ -356,14 +376,47 @@ int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k
   a.head_dim = static_cast<int>(head_dim);
   a.scale = scale;
   a.decode_ctas = ctas;
-  a.decode_kernel = decode_kernel_choice();
-  a.prefill_kernel = prefill_kernel_choice();
-  a.overlap = overlap_choice();
+  a.decode_kernel = (opt && opt->decode_kernel) ? opt->decode_kernel : decode_kernel_choice();
+  a.prefill_kernel = (opt && opt->prefill_kernel) ? opt->prefill_kernel : prefill_kernel_choice();
+  a.overlap = (opt && opt->overlap) ? (opt->overlap == 1 ? 1 : 0) : overlap_choice();
   a.fault = fault_injection_choice();
+  a.side_stream = opt ? static_cast<cudaStream_t>(opt->side_stream) : nullptr;
+  a.fork_event = opt ? static_cast<cudaEvent_t>(opt->fork_event) : nullptr;
+  a.join_event = opt ? static_cast<cudaEvent_t>(opt->join_event) : nullptr;
   a.plan = plan_view(workspace, ps);
   a.max_tiles = ps.max_tiles;
   a.err = g_err_ptr[dev];
   return launch_paged_attention(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_paged_attention(const void* q, int64_t q_st, int64_t q_sh, const void* k_cache,
+                        const void* v_cache, int64_t num_blocks, int64_t block_size,
+                        const int32_t* block_tables, int64_t bt_stride, int64_t max_blocks_per_seq,
+                        const int32_t* context_lens, const int32_t* query_start_loc, int64_t num_seqs,
+                        void* out, int64_t o_st, int64_t o_sh, int64_t num_tokens, int64_t num_q_heads,
+                        int64_t num_kv_heads, int64_t head_dim, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return paged_attention_impl(q, q_st, q_sh, k_cache, v_cache, num_blocks, block_size, block_tables, bt_stride,
+                              max_blocks_per_seq, context_lens, query_start_loc, num_seqs, out, o_st, o_sh,
+                              num_tokens, num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
+                              stream, nullptr);
+}
+
+int pkv_paged_attention_ex(const void* q, int64_t q_st, int64_t q_sh, const void* k_cache,
+                           const void* v_cache, int64_t num_blocks, int64_t block_size,
+                           const int32_t* block_tables, int64_t bt_stride, int64_t max_blocks_per_seq,
+                           const int32_t* context_lens, const int32_t* query_start_loc, int64_t num_seqs,
+                           void* out, int64_t o_st, int64_t o_sh, int64_t num_tokens, int64_t num_q_heads,
+                           int64_t num_kv_heads, int64_t head_dim, float scale, void* workspace,
+                           size_t workspace_bytes, void* stream, const pkv_attention_options* options) {
+  return paged_attention_impl(q, q_st, q_sh, k_cache, v_cache, num_blocks, block_size, block_tables, bt_stride,
+                              max_blocks_per_seq, context_lens, query_start_loc, num_seqs, out, o_st, o_sh,
+                              num_tokens, num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
+                              stream, options);
 }
 
 int pkv_get_device_error(uint32_t* bits, int clear, void* stream) {

@@ -444,10 +444,38 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   const int sms = device_sm_count();
   const int64_t pf_grid = use_tc ? prefill_tc_grid(a, tcp.prows) : prefill_mma_grid(a);
   // Prefill beside the decode: only with spans of two or more tokens (more tokens than
-  // sequences), the tcgen05 tiles (one CTA per SM) and the default one decode CTA per SM.
+  // sequences), the tcgen05 tiles (one CTA per SM) and the default one decode CTA per SM, on
+  // the caller's second stream (with its fork/join events) or else the library's own.
   SideStream side{};
-  const bool split = a.overlap && use_tc && a.num_tokens > a.num_seqs && a.decode_ctas == sms && sms > 1 &&
-                     side_stream_for_device(&side);
+  bool split = a.overlap && use_tc && a.num_tokens > a.num_seqs && a.decode_ctas == sms && sms > 1;
+  const bool own_side = split && a.side_stream == nullptr;
+  if (split && !own_side) {
+    side.stream = a.side_stream;
+    side.fork = a.fork_event;
+    side.join = a.join_event;
+  } else if (own_side) {
+    split = side_stream_for_device(&side);
+  }
+  // The library's side stream is shared by every caller on the device; its use, from this
+  // check to the join, is serialised by a host mutex.  Through the fork event it joins a graph
+  // capture of the caller's stream and stays in that capture until the capture ends, so it
+  // is taken only when no capture holds it, or when the capture holding it is this call's;
+  // otherwise this call runs in the serial order.
+  std::unique_lock<std::mutex> hold;
+  if (split && own_side) {
+    hold = std::unique_lock<std::mutex>(*static_cast<std::mutex*>(side.lock));
+    cudaStreamCaptureStatus st_side = cudaStreamCaptureStatusNone, st_call = cudaStreamCaptureStatusNone;
+    unsigned long long id_side = 0, id_call = 0;
+    if (cudaStreamGetCaptureInfo(side.stream, &st_side, &id_side) != cudaSuccess ||
+        cudaStreamGetCaptureInfo(stream, &st_call, &id_call) != cudaSuccess) {
+      split = false;
+    } else if (st_side != cudaStreamCaptureStatusNone &&
+               !(st_side == cudaStreamCaptureStatusActive && st_call == cudaStreamCaptureStatusActive &&
+                 id_side == id_call)) {
+      split = false;
+    }
+    if (!split) hold.unlock();
+  }
   SplitArgs sp{};
   sp.on = split ? 1 : 0;
   sp.sms = sms;
@@ -493,7 +521,6 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
     return decode();
   }
   // fork after the planner, decode here, prefill on the side stream, join before returning
-  std::lock_guard<std::mutex> hold(*static_cast<std::mutex*>(side.lock));
   if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess) return e;
   if ((e = decode()) != cudaSuccess) return e;
   if ((e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess) return e;

@@ -129,6 +129,8 @@ struct AttnArgs {
   int prefill_kernel;  // 1 mma.sync tiles, 2 tcgen05 tiles (resolved from the process setting)
   int overlap;         // 1: prefill tiles run beside the decode on a second stream (SMs split)
   int fault;           // test-only fault injection (pkv_set_fault_injection); 0 in normal use
+  cudaStream_t side_stream;  // the caller's second stream for the prefill beside the decode, or null
+  cudaEvent_t fork_event, join_event;  // (with it) the caller's events ordering that stream
   Plan plan;
   int64_t max_tiles;
   unsigned int* err;

@@ -139,25 +139,59 @@ def rope_turn_table(rope_theta, head_dim):
     return np.frombuffer(out, dtype=np.uint64)[: int(head_dim) // 2].copy()
 
 
-def workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq):
-    """Bytes of workspace ``paged_attention`` needs (``pkv_paged_attention_workspace_size``)."""
-    n = _lib.load().pkv_paged_attention_workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads,
-                                                       head_dim, max_blocks_per_seq)
+def workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, decode_ctas=0):
+    """Bytes of workspace ``paged_attention`` needs (``pkv_paged_attention_workspace_size_ex``;
+    ``decode_ctas`` as the per-call option, 0 for the process default)."""
+    n = _lib.load().pkv_paged_attention_workspace_size_ex(num_tokens, num_seqs, num_q_heads, num_kv_heads,
+                                                          head_dim, max_blocks_per_seq, int(decode_ctas))
     if n == 0:
         raise ValueError("invalid sizes for paged_attention")
     return int(n)
 
 
 def alloc_workspace(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                    device=None):
-    n = workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq)
-    # 256-byte alignment: torch's caching allocator returns 512-byte aligned blocks
+                    device=None, decode_ctas=0):
+    """A caller-owned workspace tensor (uint8) of the required size on `device` (default: the
+    current CUDA device); torch's caching allocator returns 512-byte aligned blocks."""
+    n = workspace_size(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, decode_ctas)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
+_OVERLAP = {None: 0, True: 1, False: 2}
+
+
+def _options(options):
+    """A pkv_attention_options from a dict: decode_kernel ('auto' | 'simt' | 'tensor'),
+    prefill_kernel ('auto' | 'mma' | 'tcgen05'), overlap (None | True | False), decode_ctas (int),
+    side_stream (torch.cuda.Stream) with fork_event and join_event (torch.cuda.Event)."""
+    if options is None:
+        return None
+    unknown = set(options) - {"decode_kernel", "prefill_kernel", "overlap", "decode_ctas", "side_stream",
+                              "fork_event", "join_event"}
+    if unknown:
+        raise ValueError(f"unknown options {sorted(unknown)}")
+    opt = _lib.AttentionOptions()
+    opt.struct_size = ctypes.sizeof(_lib.AttentionOptions)
+    opt.decode_kernel = DECODE_KERNELS[options.get("decode_kernel", "auto")]
+    opt.prefill_kernel = PREFILL_KERNELS[options.get("prefill_kernel", "auto")]
+    opt.overlap = _OVERLAP[options.get("overlap", None)]
+    opt.decode_ctas = int(options.get("decode_ctas", 0))
+    side = options.get("side_stream")
+    if side is not None:
+        fork, join = options.get("fork_event"), options.get("join_event")
+        for ev in (fork, join):  # torch creates an event's CUDA handle at its first record
+            if ev is not None and not ev.cuda_event:
+                ev.record(side)
+        opt.side_stream = ctypes.c_void_p(side.cuda_stream)
+        opt.fork_event = ctypes.c_void_p(fork.cuda_event) if fork is not None else None
+        opt.join_event = ctypes.c_void_p(join.cuda_event) if join is not None else None
+    return opt
+
+
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, out=None,
-                    workspace=None, max_blocks_per_seq=None, stream=None):
-    """Paged GQA over a ragged prefill/decode batch (``pkv_paged_attention``).  Returns out."""
+                    workspace=None, max_blocks_per_seq=None, stream=None, options=None):
+    """Paged GQA over a ragged prefill/decode batch (``pkv_paged_attention``, or with per-call
+    ``options`` -- a dict, see ``_options`` -- ``pkv_paged_attention_ex``).  Returns out."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
@@ -183,16 +217,20 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, query_start
     _need(out, "out", torch.bfloat16, 3)
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")
+    opt = _options(options)
     if workspace is None:
-        workspace = alloc_workspace(T, B, hq, hkv, d, mb, device=q.device)
+        workspace = alloc_workspace(T, B, hq, hkv, d, mb, device=q.device,
+                                    decode_ctas=opt.decode_ctas if opt is not None else 0)
     qs, qh = _rows(q, "q")
     os_, oh = _rows(out, "out")
-    st = _lib.load().pkv_paged_attention(
-        q.data_ptr(), qs, qh, k_cache.data_ptr(), v_cache.data_ptr(), nb, bs,
-        block_tables.data_ptr(), block_tables.stride(0), mb, context_lens.data_ptr(),
-        query_start_loc.data_ptr(), B, out.data_ptr(), os_, oh, T, hq, hkv, d, float(scale),
-        workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
-    _lib.check("pkv_paged_attention", st)
+    args = (q.data_ptr(), qs, qh, k_cache.data_ptr(), v_cache.data_ptr(), nb, bs,
+            block_tables.data_ptr(), block_tables.stride(0), mb, context_lens.data_ptr(),
+            query_start_loc.data_ptr(), B, out.data_ptr(), os_, oh, T, hq, hkv, d, float(scale),
+            workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    if opt is None:
+        _lib.check("pkv_paged_attention", _lib.load().pkv_paged_attention(*args))
+    else:
+        _lib.check("pkv_paged_attention_ex", _lib.load().pkv_paged_attention_ex(*args, ctypes.byref(opt)))
     return out
 
 

@@ -152,3 +152,32 @@ def test_copy_host_validation(lib):
     assert lib.pkv_copy(264, 256, 64, None) == 4  # dst not 16-byte aligned
     assert lib.pkv_copy(256, 256, 60, None) == 4  # size not a multiple of 16
 
+
+
+def _attn_ex_args(x, opt_ptr):
+    # a valid-looking call; the option checks come before anything touches the GPU
+    return [x, 1024, 128, x, x, 10, 16, x, 8, 8, x, x, 2, x, 1024, 128, 2, 8, 4, 128, ctypes.c_float(0.1),
+            x, 1 << 20, None, opt_ptr]
+
+
+def test_attention_options_are_validated_on_the_host(lib):
+    x = ctypes.c_void_p(256)
+    opt = _lib.AttentionOptions()
+    opt.struct_size = ctypes.sizeof(_lib.AttentionOptions) + 4  # another layout
+    assert lib.pkv_paged_attention_ex(*_attn_ex_args(x, ctypes.byref(opt))) == 2  # PKV_ERR_SHAPE
+    for field, value in [("decode_kernel", 3), ("prefill_kernel", -1), ("overlap", 3), ("decode_ctas", -1),
+                         ("decode_ctas", (1 << 16) + 1)]:
+        opt = _lib.AttentionOptions()
+        opt.struct_size = ctypes.sizeof(_lib.AttentionOptions)
+        setattr(opt, field, value)
+        assert lib.pkv_paged_attention_ex(*_attn_ex_args(x, ctypes.byref(opt))) == 2, field
+    opt = _lib.AttentionOptions()
+    opt.struct_size = ctypes.sizeof(_lib.AttentionOptions)
+    opt.side_stream = 16  # a stream without its fork and join events
+    assert lib.pkv_paged_attention_ex(*_attn_ex_args(x, ctypes.byref(opt))) == 1  # PKV_ERR_NULL
+
+
+def test_workspace_size_ex_rejects_bad_decode_grids(lib):
+    assert lib.pkv_paged_attention_workspace_size_ex(4, 4, 8, 4, 128, 8, -1) == 0
+    assert lib.pkv_paged_attention_workspace_size_ex(4, 4, 8, 4, 128, 8, (1 << 16) + 1) == 0
+    assert lib.pkv_paged_attention_workspace_size_ex(4, 4, 8, 4, 96, 8, 7) == 0

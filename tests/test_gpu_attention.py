@@ -448,3 +448,76 @@ def test_prefill_rows_without_more_tokens_than_sequences(case, decode_kernel):
     torch.cuda.synchronize()
     header = ws[:16].cpu().numpy().view(np.int32)[:4].tolist()
     assert header[0] == sum(spans) and header[3] == 0
+
+
+@pytest.mark.parametrize("opts", [
+    {"decode_kernel": "simt"}, {"decode_kernel": "tensor", "decode_ctas": 7},
+    {"prefill_kernel": "mma"}, {"overlap": False}, {"overlap": True, "prefill_kernel": "tcgen05"},
+])
+def test_per_call_options_equal_the_process_settings(opts, overlap_setting):
+    # pkv_paged_attention_ex: the same kernels and split as the process-wide settings give
+    bt, q_rot, kc, vc, ref = config_with_oracle(5)
+    d = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
+    got = ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                              options=opts)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    try:
+        if "decode_kernel" in opts:
+            ops.set_decode_kernel(opts["decode_kernel"])
+        if "prefill_kernel" in opts:
+            ops.set_prefill_kernel(opts["prefill_kernel"])
+        if "overlap" in opts:
+            ops.set_overlap(opts["overlap"])
+        if "decode_ctas" in opts:
+            ops.set_decode_ctas(opts["decode_ctas"])
+        want = d.attend()
+        torch.cuda.synchronize()
+    finally:
+        ops.set_decode_kernel("auto")
+        ops.set_prefill_kernel("auto")
+        ops.set_decode_ctas(0)
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert_close(got.float().cpu().numpy(), ref, f"options {opts}")
+
+
+def test_caller_side_stream_gives_the_same_result():
+    # the prefill beside the decode on the caller's own second stream and events
+    bt, q_rot, kc, vc, ref = config_with_oracle(5)
+    d = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
+    lib_side = d.attend()
+    side = torch.cuda.Stream()
+    opts = {"side_stream": side, "fork_event": torch.cuda.Event(), "join_event": torch.cuda.Event()}
+    own_side = ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                                   options=opts)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    assert torch.equal(own_side.view(torch.int16), lib_side.view(torch.int16))
+    assert_close(own_side.float().cpu().numpy(), ref, "caller side stream")
+
+
+def test_eager_call_on_another_stream_while_a_capture_is_open():
+    # a capture of stream A pulls the library's second stream into its graph until the capture
+    # ends; an eager call on stream B meanwhile must not use it (it runs in the serial order)
+    bt, q_rot, kc, vc, ref = config_with_oracle(5)
+    d = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
+    d.attend()  # one-time per-device set-up outside the capture
+    mk = lambda: ops.alloc_workspace(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads,  # noqa: E731
+                                     bt.head_dim, bt.block_tables.shape[1])
+    ws_a, ws_b = mk(), mk()
+    out_a, out_b = torch.empty_like(d.q), torch.full_like(d.q, float("nan"))
+    other = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                            out=out_a, workspace=ws_a)
+        with torch.cuda.stream(other):
+            ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                                out=out_b, workspace=ws_b)
+    torch.cuda.synchronize()
+    assert_close(out_b.float().cpu().numpy(), ref, "eager call during another stream's capture")
+    g.replay()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    assert_close(out_a.float().cpu().numpy(), ref, "captured call")
