@@ -151,6 +151,64 @@ def time_oracle(bt, budget_s=12.0, min_seqs=2):
         n = min(bt.num_seqs, max(n + 1, int(n * min(8.0, (budget_s / 4) / max(dt, 1e-3)))))
 
 
+# ------------------------------------------------------------- the oracle on all host cores
+def _oracle_worker(conn):
+    """A worker process: receives its sub-batch once, then runs the oracle on it per request
+    and answers (wall seconds, CPU seconds)."""
+    sb = conn.recv()
+    while conn.recv() is not None:
+        c0, t0 = time.process_time(), time.perf_counter()
+        oracle_step(sb)
+        conn.send((time.perf_counter() - t0, time.process_time() - c0))
+
+
+class OracleWorkers:
+    """The oracle over the first `n` sequences, split by sequence (they are independent) into
+    one sub-batch per worker process.  Processes start with `spawn`: the parent may already
+    hold a CUDA context, which a forked child must not inherit.  A step sends every worker
+    its run request and waits for all answers, so its wall time is the parallel pass."""
+
+    def __init__(self, bt, n, procs):
+        import multiprocessing as mp
+
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ.setdefault(var, "1")  # one thread per worker; the children inherit it
+        ctx = mp.get_context("spawn")
+        chunks = [c for c in np.array_split(np.arange(n), max(1, procs)) if len(c)]
+        self.conns, self.procs = [], []
+        for c in chunks:
+            mine, theirs = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(theirs,), daemon=True)
+            p.start()
+            mine.send(sub_batch(bt, [int(x) for x in c]))
+            self.conns.append(mine)
+            self.procs.append(p)
+
+    def step(self):
+        """(wall seconds, CPU seconds summed over the workers) of one parallel pass."""
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send(1)
+        answers = [c.recv() for c in self.conns]
+        return time.perf_counter() - t0, sum(a[1] for a in answers)
+
+    def close(self):
+        for c in self.conns:
+            c.send(None)
+        for p in self.procs:
+            p.join(timeout=30)
+
+
+def parallel_oracle(bt, budget_s, procs):
+    """Workers over a sample sized so that a parallel pass costs about budget/4 (estimated from
+    a short serial pass).  Returns (workers, sample size, unique KV bytes of the sample)."""
+    _, dt, n0, _ = time_oracle(bt, budget_s=min(budget_s, 4.0) / 4)
+    per_seq = dt / n0
+    n = int(min(bt.num_seqs, max(n0, procs * (budget_s / 4) / max(per_seq, 1e-6))))
+    workers = OracleWorkers(bt, n, procs)
+    return workers, n, kv_unique_bytes(sub_batch(bt, range(n)))
+
+
 # ------------------------------------------------------------------------------ clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -641,16 +699,23 @@ def run_gpu(args, rank, world, local_rank):
         "decode_seqs": n_decode,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        sb, dt, n, used = time_oracle(bt, budget_s=args.cpu_budget)
-        kv_s = kv_unique_bytes(sb)
+        procs = host_cores()
+        workers, n, kv_s = parallel_oracle(bt, args.cpu_budget, procs)
+        try:
+            workers.step()  # warm-up: imports and first touch in every worker
+            dt, cpu = workers.step()
+        finally:
+            workers.close()
         line["cpu_baseline"] = {
             "value": round(kv_s / dt / 1e9, 4),
             "unit": UNIT,
-            "cores": used,
-            "cores_available": host_cores(),
+            "cores": threads_used(cpu, dt),
+            "cores_available": procs,
+            "workers": len(workers.procs),
             "kind": "oracle",
             "sample": f"first {n} of {bt.num_seqs} sequences of {bt.name} ({kv_s / 1e6:.1f} MB unique KV), "
-                      f"oracle kv_append + paged_attention, one pass {dt:.2f} s",
+                      f"oracle kv_append + paged_attention split by sequence over {len(workers.procs)} "
+                      f"worker processes, one parallel pass {dt:.3f} s",
         }
     if dist:
         dist.destroy_process_group()
@@ -660,17 +725,19 @@ def run_gpu(args, rank, world, local_rank):
 # ----------------------------------------------------------------------- reference arm
 def run_reference(args):
     bt = W.config(args.workload, poison=False, block_size=args.block_size)
-    sb, dt, n, _ = time_oracle(bt, budget_s=min(args.cpu_budget, 8.0))
-    kv_s = kv_unique_bytes(sb)
-    for _ in range(args.warmup):
-        oracle_step(sb)
-    times = []
-    c0 = time.process_time()
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oracle_step(sb)
-        times.append(time.perf_counter() - t0)
-    used = threads_used(time.process_time() - c0, sum(times))
+    procs = host_cores()
+    workers, n, kv_s = parallel_oracle(bt, min(args.cpu_budget, 8.0), procs)
+    times, cpus = [], []
+    try:
+        for _ in range(args.warmup):
+            workers.step()
+        for _ in range(args.steps):
+            dt, cpu = workers.step()
+            times.append(dt)
+            cpus.append(cpu)
+    finally:
+        workers.close()
+    used = threads_used(sum(cpus), sum(times))
     ms = 1e3 * sum(times) / len(times)
     value = round(kv_s / (ms * 1e-3) / 1e9, 4)
     return {
@@ -694,7 +761,9 @@ def run_reference(args):
             "cores": used,
             "cores_available": host_cores(),
             "kind": "oracle",
-            "sample": f"first {n} of {bt.num_seqs} sequences of {bt.name} per step ({kv_s / 1e6:.1f} MB unique KV)",
+            "workers": len(workers.procs),
+            "sample": f"first {n} of {bt.num_seqs} sequences of {bt.name} per step ({kv_s / 1e6:.1f} MB unique KV), "
+                      f"split by sequence over {len(workers.procs)} worker processes",
         },
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
