@@ -24,7 +24,7 @@ special cases).  Every function here is pinned; none is "parity unpinned".
 
 from .bf16 import bf16_bits_to_f64, f64_to_bf16_bits
 from .rope import rope_inv_freq, rope64
-from .append import kv_append
+from .append import kv_append, positions_and_slots
 from .attention import (
     paged_attention,
     gather_sequence_kv,
@@ -40,6 +40,7 @@ __all__ = [
     "rope_inv_freq",
     "rope64",
     "kv_append",
+    "positions_and_slots",
     "paged_attention",
     "gather_sequence_kv",
     "attention_partial",

@@ -56,3 +56,26 @@ def kv_append(q, k, v, positions, slot_mapping, k_cache, v_cache, rope_theta):
         kc[blk, off] = k_rot[t]
         vc[blk, off] = v[t]
     return f64_to_bf16_bits(q_rot64), kc, vc
+
+
+def positions_and_slots(query_start_loc, context_lens, block_tables, block_size, num_tokens):
+    """Where each new token sits and which pool slot it is written to, from the scheduler's
+    tables ("09 -- Mini Inference Engine (The Capstone)", "Week 4 -- Paged KV cache": logical
+    block i of a sequence is physical block ``block_table[i]``; the reading of the slot number
+    as above).  Token t of sequence b's span (rows ``[qsl[b], qsl[b+1])``, n of them, over a
+    context of ctx keys that counts the span) sits at position ``p = ctx - n + (t - qsl[b])``
+    and goes to slot ``block_tables[b][p // bs] * bs + p % bs``.  Tokens outside every span
+    get position 0 and slot -1.  Returns int64 arrays (positions, slots) of length num_tokens.
+    """
+    qsl = np.asarray(query_start_loc).astype(np.int64)
+    ctx = np.asarray(context_lens).astype(np.int64)
+    positions = np.zeros(int(num_tokens), dtype=np.int64)
+    slots = np.full(int(num_tokens), -1, dtype=np.int64)
+    for b in range(len(ctx)):
+        n = int(qsl[b + 1] - qsl[b])
+        for r in range(n):
+            t = int(qsl[b]) + r
+            p = int(ctx[b]) - n + r
+            positions[t] = p
+            slots[t] = int(block_tables[b][p // block_size]) * block_size + p % block_size
+    return positions, slots

@@ -133,7 +133,7 @@ const char* pkv_status_string(int status) {
   }
 }
 
-int pkv_version(void) { return 100; }
+int pkv_version(void) { return 200; }
 
 int pkv_set_overlap(int on) {
   if (on != 0 && on != 1) return PKV_ERR_SHAPE;

@@ -115,8 +115,10 @@ def test_append_with_device_side_slots_matches_explicit_slots(index):
                         bt.rope_theta, positions_out=pos, slot_mapping_out=slots)
     torch.cuda.synchronize()
     assert ops.get_device_error() == 0
-    assert np.array_equal(pos.cpu().numpy(), bt.positions)
-    assert np.array_equal(slots.cpu().numpy(), bt.slot_mapping)
+    want_pos, want_slots = oracle.positions_and_slots(bt.query_start_loc, bt.context_lens, bt.block_tables,
+                                                      bt.block_size, bt.num_tokens)
+    assert np.array_equal(pos.cpu().numpy(), want_pos)
+    assert np.array_equal(slots.cpu().numpy(), want_slots)
     for a, b in ((d.k_cache, ref.k_cache), (d.v_cache, ref.v_cache), (d.q, ref.q)):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
@@ -136,8 +138,10 @@ def test_device_side_slots_skip_tokens_outside_spans():
                         bt.rope_theta, positions_out=pos, slot_mapping_out=slots)
     torch.cuda.synchronize()
     assert ops.get_device_error() == 0
-    assert np.array_equal(slots.cpu().numpy()[:T], bt.slot_mapping)
-    assert np.array_equal(pos.cpu().numpy()[:T], bt.positions)
+    want_pos, want_slots = oracle.positions_and_slots(bt.query_start_loc, bt.context_lens, bt.block_tables,
+                                                      bt.block_size, T + 2)
+    assert np.array_equal(slots.cpu().numpy(), want_slots)
+    assert np.array_equal(pos.cpu().numpy(), want_pos)
     assert np.all(slots.cpu().numpy()[T:] == -1)
     q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
                                      bt.rope_theta)

@@ -180,3 +180,38 @@ def test_append_then_single_key_attention_returns_v():
     for t in range(3):
         for h in range(6):
             assert np.array_equal(out[t, h], oracle.bf16_bits_to_f64(bt.v[t, h // G]))
+
+
+def test_positions_and_slots_on_a_hand_example():
+    # block size 4; sequence 0: 6 keys, a 2-row span (positions 4, 5) in logical block 1 ->
+    # physical 7; sequence 1: empty span; sequence 2: 3 keys, one decode row (position 2) in
+    # logical block 0 -> physical 2; a trailing token no span covers
+    tables = np.array([[3, 7], [5, -1], [2, -1]])
+    pos, slots = oracle.positions_and_slots([0, 2, 2, 3], [6, 9, 3], tables, 4, 4)
+    assert pos.tolist() == [4, 5, 2, 0]
+    assert slots.tolist() == [7 * 4 + 0, 7 * 4 + 1, 2 * 4 + 2, -1]
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_positions_and_slots_reproduce_the_workloads(index):
+    # the generator places the new tokens as a scheduler would; its explicit positions and
+    # slots agree with the derivation from the tables, and every slot is inside the pool and
+    # unique
+    bt = W.config(index, poison=False)
+    pos, slots = oracle.positions_and_slots(bt.query_start_loc, bt.context_lens, bt.block_tables,
+                                            bt.block_size, bt.num_tokens)
+    assert np.array_equal(pos, bt.positions) and np.array_equal(slots, bt.slot_mapping)
+    assert np.all((slots >= 0) & (slots < bt.num_blocks * bt.block_size))
+    assert len(set(slots.tolist())) == len(slots)
+
+
+def test_positions_and_slots_follow_the_block_table_not_the_position():
+    # permuting the physical blocks moves the slots with them; positions do not change
+    bt = W.config(2, poison=False)
+    perm = np.random.default_rng(1).permutation(bt.num_blocks)
+    tables = np.where(bt.block_tables >= 0, perm[np.maximum(bt.block_tables, 0)], -1)
+    pos, slots = oracle.positions_and_slots(bt.query_start_loc, bt.context_lens, tables, bt.block_size,
+                                            bt.num_tokens)
+    assert np.array_equal(pos, bt.positions)
+    blk, off = np.divmod(bt.slot_mapping, bt.block_size)
+    assert np.array_equal(slots, perm[blk] * bt.block_size + off)
