@@ -92,7 +92,7 @@ bool encode_bf16_sw128(CUtensorMap* m, const void* base, int rank, const cuuint6
 
 // The pool [num_blocks][block_size][Hkv][d] as a 4-D tensor {d, Hkv, block_size, num_blocks};
 // a box is all block_size token rows x 64 dims of one kv head in one block, 128-byte swizzled
-// (the tcgen05 prefill's K tiles).
+// (the tcgen05 prefill's K/V tiles).
 bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_log2, int hkv, int D) {
   const cuuint64_t bs = cuuint64_t(1) << bs_log2;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv), bs,
@@ -391,7 +391,8 @@ bool make_q_map(CUtensorMap* m, const AttnArgs& a) {
 bool make_prefill_tc_params(const AttnArgs& a, PrefillTcParams* P) {
   if (a.q_sh <= 0 || a.q_st <= 0) return false;
   if (!make_q_map(&P->tmap_q, a) ||
-      !make_pool_map(&P->tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, a.head_dim))
+      !make_pool_map(&P->tmap_k, a.k_cache, a.num_blocks, a.bs_log2, a.hkv, a.head_dim) ||
+      !make_pool_map(&P->tmap_v, a.v_cache, a.num_blocks, a.bs_log2, a.hkv, a.head_dim))
     return false;
   P->p = make_prefill_params(a);
   P->group = a.hq / a.hkv;
@@ -412,8 +413,7 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcParams& P, cudaS
   if (const cudaError_t e = set_smem_once<prefill_tc_kernel<D>>(C::kSmemBytes); e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(prefill_tc_grid(a, P.prows));
   record_kernel_event(PKV_KERNEL_PREFILL, false, stream);
-  const cudaError_t e =
-      launch_kernel(pdl, prefill_tc_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, P);
+  const cudaError_t e = launch_kernel(pdl, prefill_tc_kernel<D>, dim3(grid), dim3(256), C::kSmemBytes, stream, P);
   record_kernel_event(PKV_KERNEL_PREFILL, true, stream);
   return e;
 }
