@@ -417,9 +417,13 @@ def run_gpu(args, rank, world, local_rank):
                              bt.block_tables.shape[1], device=dev)
     stream = torch.cuda.current_stream()
 
+    # the step's kv_append sits between the index tables' upload and the attention call, so the
+    # planner may do its arithmetic while the append runs (PKV_ATTN_PLAN_EARLY)
+    attn_opts = ops.attention_options({"plan_early": not args.no_plan_early})
+
     def step():
         ops.kv_append(q, k, v, pos, slots, kc, vc, bt.rope_theta)
-        ops.paged_attention(q, kc, vc, tables, ctx, qsl, bt.scale, out=out, workspace=ws)
+        ops.paged_attention(q, kc, vc, tables, ctx, qsl, bt.scale, out=out, workspace=ws, options=attn_opts)
 
     for _ in range(args.warmup):
         step()
@@ -573,7 +577,7 @@ def run_gpu(args, rank, world, local_rank):
             stg.upload(stream)
             ops.kv_append(sd.q, sd.k, sd.v, sd.positions, sd.slot_mapping, kc, vc, bt.rope_theta)
             ops.paged_attention(sd.q, kc, vc, sd.block_tables, sd.context_lens, sd.query_start_loc, bt.scale,
-                                out=out, workspace=ws)
+                                out=out, workspace=ws, options=attn_opts)
             if kernel_copy:
                 ops.copy(host_out, out)
             else:
@@ -585,7 +589,7 @@ def run_gpu(args, rank, world, local_rank):
         ops.kv_append(sd.q, sd.k, sd.v, sd.positions, sd.slot_mapping, kc, vc, bt.rope_theta)
         stream.wait_event(out_free[j])
         ops.paged_attention(sd.q, kc, vc, sd.block_tables, sd.context_lens, sd.query_start_loc, bt.scale,
-                            out=outs[j], workspace=ws)
+                            out=outs[j], workspace=ws, options=attn_opts)
         out_ready[j].record(stream)
         d2h_stream.wait_event(out_ready[j])
         if kernel_copy:
@@ -642,6 +646,7 @@ def run_gpu(args, rank, world, local_rank):
             "decode_kernel": args.decode_kernel,
             "prefill_kernel": args.prefill_kernel,
             "prefill_beside_decode": not args.no_overlap,
+            "plan_early": not args.no_plan_early,
             "l2": ("L2 flushed between timed steps (unique KV per step %.1f MB < 2 x 129 MB): a %d MiB "
                    "scratch write before each step, each step timed alone with CUDA events"
                    % (kv_u / 1e6, FLUSH_BYTES >> 20)) if flush else
@@ -784,6 +789,8 @@ def main():
     ap.add_argument("--seqs", type=int, default=0, help="only the first N sequences (small profiling case)")
     ap.add_argument("--decode-kernel", choices=["auto", "simt", "tensor"], default="auto")
     ap.add_argument("--prefill-kernel", choices=["auto", "mma", "tcgen05"], default="auto")
+    ap.add_argument("--no-plan-early", action="store_true",
+                    help="plan after the append has finished (default: the planner computes while it runs)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="prefill tiles before the decode on one stream (default: beside it, SMs split)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

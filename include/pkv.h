@@ -233,6 +233,14 @@ PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64
  *   overlap         0 default, 1 prefill tiles beside the decode when possible, 2 serial order
  *   decode_ctas     0 default, else the decode grid of this call (1 .. 65536); the workspace
  *                   must then hold pkv_paged_attention_workspace_size_ex(..., decode_ctas)
+ *   flags           0, or PKV_ATTN_PLAN_EARLY: the planner reads query_start_loc and
+ *                   context_lens, and does all its arithmetic, while the work enqueued just
+ *                   before this call may still be running, and writes the workspace only once
+ *                   that work has finished; a decode step then hides the planner behind its
+ *                   pkv_kv_append.  Set it only when that work neither writes these two arrays
+ *                   nor lets later work start before their writer has finished: the step's
+ *                   pkv_kv_append qualifies (it waits for all earlier work before it lets later
+ *                   work start).  Batches of more than 1024 sequences ignore the flag.
  *   side_stream, fork_event, join_event
  *                   all NULL: the library's own second stream for the prefill beside the
  *                   decode; else a caller-owned stream (cudaStream_t) and two caller-created
@@ -240,15 +248,17 @@ PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64
  *                   back into `stream` -- independent callers on different streams then never
  *                   share, or serialise on, a stream of the library's.  The caller must not
  *                   use them for anything else until the call's work has completed.
- * Invalid values give PKV_ERR_SHAPE; one or two of the three handles given give PKV_ERR_NULL.
+ * Invalid values (unknown flag bits included) give PKV_ERR_SHAPE; one or two of the three
+ * handles given give PKV_ERR_NULL.
  */
+#define PKV_ATTN_PLAN_EARLY 1
 typedef struct pkv_attention_options {
   uint32_t struct_size;
   int32_t decode_kernel;
   int32_t prefill_kernel;
   int32_t overlap;
   int32_t decode_ctas;
-  int32_t reserved;  /* 0 */
+  int32_t flags;  /* PKV_ATTN_* bits */
   void* side_stream;
   void* fork_event;
   void* join_event;

@@ -87,7 +87,7 @@ class AttentionOptions(ctypes.Structure):
 
     _fields_ = [("struct_size", ctypes.c_uint32), ("decode_kernel", ctypes.c_int32),
                 ("prefill_kernel", ctypes.c_int32), ("overlap", ctypes.c_int32),
-                ("decode_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("decode_ctas", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("side_stream", ctypes.c_void_p), ("fork_event", ctypes.c_void_p),
                 ("join_event", ctypes.c_void_p)]
 

@@ -330,6 +330,166 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   }
 }
 
+// The same plan for a batch of at most kPlanThreads sequences, one thread per sequence,
+// computed in registers and shared memory first and written to the workspace at the end.
+// With `early` the arithmetic runs before the wait on the previous kernel (only the inputs
+// query_start_loc and context_lens are read by then; the caller vouches that the kernel
+// before this call does not write them) and only the workspace writes come after it, so the
+// planner's work overlaps that kernel (the step's kv_append).  Without `early` it waits
+// first, like plan_kernel.
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel_small(const int32_t* __restrict__ qsl,
+                                                                  const int32_t* __restrict__ ctxl,
+                                                                  int num_seqs, int64_t num_tokens,
+                                                                  int64_t max_ctx, int pps, int decode_ctas,
+                                                                  int tile_q, Plan plan, int64_t max_tiles,
+                                                                  SplitArgs split, int rows_in_decode, int early,
+                                                                  unsigned int* err) {
+  __shared__ int sm[3 * 32];
+  __shared__ unsigned long long pf_keytiles;  // 128-key tiles over all prefill q tiles (one kv head)
+  __shared__ int pf_maxtile;                  // the most key tiles of one q tile
+  __shared__ unsigned long long best;         // (cost bits << 32) | prefill CTAs
+  if (threadIdx.x == 0) {
+    pf_keytiles = 0;
+    pf_maxtile = 0;
+    best = ~0ull;
+  }
+  if (early) {
+    pdl_trigger();  // the decode may start its prologue; it waits for this kernel's end
+  } else {
+    pdl_wait();  // the workspace may still be read by the previous call's kernels until now
+    pdl_trigger();
+  }
+  __syncthreads();
+  // this thread's sequence: decode entries (a), work units (b), prefill q tiles (c)
+  const int b = threadIdx.x;
+  int s0 = 0, span = 0, ctx = 0;
+  Int3 v = {0, 0, 0};
+  if (b < num_seqs) {
+    s0 = qsl[b];
+    const int s1 = qsl[b + 1];
+    ctx = ctxl[b];
+    span = s1 - s0;
+    bool ok = s0 >= 0 && span >= 0 && s1 <= num_tokens;
+    if (!ok) {
+      raise_error(err, PKV_DEVERR_SPAN);
+    } else if (span > 0) {
+      if (ctx < span) {
+        raise_error(err, PKV_DEVERR_SPAN);
+        ok = false;
+      } else if (static_cast<int64_t>(ctx) > max_ctx) {  // more keys than the table row maps
+        raise_error(err, PKV_DEVERR_CONTEXT);
+        ok = false;
+      }
+    }
+    if (ok && (span == 1 || (span > 1 && rows_in_decode))) {
+      // one decode entry per row: row r sees keys 0 .. ctx - span + r
+      v.a = span;
+      for (int r = 0; r < span; ++r) v.b += ceil_div(ceil_div(ctx - span + r + 1, kPageTokens), pps);
+    }
+    if (ok && span > 1 && !rows_in_decode) {
+      v.c = ceil_div(span, tile_q);
+      if (split.on) {  // keys [0, kv_end) of q tile j are read in 128-key tiles
+        unsigned long long sum = 0;
+        int mx = 0;
+        for (int j = 0; j < v.c; ++j) {
+          const int nk = ceil_div(ctx - span + min((j + 1) * tile_q, span), 128);
+          sum += static_cast<unsigned long long>(nk);
+          mx = max(mx, nk);
+        }
+        atomicAdd(&pf_keytiles, sum);
+        atomicMax(&pf_maxtile, mx);
+      }
+    }
+  }
+  Int3 tot;
+  const Int3 ex = block_scan3(v, tot, sm);
+  const int n_dec = tot.a;
+  const int U = tot.b;
+  const int n_tiles = static_cast<int>(min(static_cast<int64_t>(tot.c), max_tiles));
+  // prefill CTAs that take items, and the decode CTAs the units are spread over (as plan_kernel)
+  int pn = split.pf_grid;
+  int dctas = decode_ctas;
+  if (split.on) {
+    const int64_t items = static_cast<int64_t>(n_tiles) * split.hkv;
+    int hi = static_cast<int>(min(static_cast<int64_t>(split.pf_grid), items));
+    if (U > 0) hi = min(hi, split.sms - 1);
+    if (hi <= 0) {
+      pn = 0;
+    } else if (U == 0) {
+      pn = hi;
+    } else {
+      const float kt = static_cast<float>(pf_keytiles) * static_cast<float>(split.hkv);
+      const float dec_bytes = static_cast<float>(U) * split.unit_bytes;
+      for (int p = 1 + static_cast<int>(threadIdx.x); p <= hi; p += kPlanThreads) {
+        const float t_dec = dec_bytes / fminf(split.hbm, static_cast<float>(split.sms - p) * split.dec_sm);
+        const float t_pf = fmaxf(kt / static_cast<float>(p), static_cast<float>(pf_maxtile)) * split.tile_bytes /
+                           split.pf_sm;
+        const unsigned long long key =
+            (static_cast<unsigned long long>(__float_as_uint(fmaxf(t_dec, t_pf))) << 32) | static_cast<unsigned>(p);
+        atomicMin(&best, key);
+      }
+      __syncthreads();
+      pn = static_cast<int>(best & 0xffffffffu);
+    }
+    if (U > 0) dctas = split.sms - pn;
+  }
+  const int W = max(1, ceil_div(U, max(1, dctas)));
+  // split pieces of this thread's decode entries: the decode CTAs touching each entry
+  Int3 pc = {0, 0, 0};
+  {
+    int unit = ex.b;
+    for (int r = 0; r < v.a; ++r) {
+      const int u1 = unit + ceil_div(ceil_div(ctx - v.a + r + 1, kPageTokens), pps);
+      pc.a += (u1 - 1) / W - unit / W + 1;
+      unit = u1;
+    }
+  }
+  Int3 ptot;
+  const Int3 pex = block_scan3(pc, ptot, sm);
+
+  if (early) pdl_wait();  // from here on the workspace is written
+  {
+    int unit = ex.b, slot = pex.a;
+    for (int r = 0; r < v.a; ++r) {
+      const int i = ex.a + r;
+      const int ctx_r = ctx - v.a + r + 1;
+      const int u1 = unit + ceil_div(ceil_div(ctx_r, kPageTokens), pps);
+      const int pieces = (u1 - 1) / W - unit / W + 1;
+      plan.dec_seq[i] = b;
+      plan.dec_count[i] = 0;
+      plan.dec_unit[i] = unit;
+      plan.dec_ctx[i] = ctx_r;
+      plan.dec_tq[i] = s0 + r;
+      plan.dec_slot[i] = slot;
+      plan.dec_chunks[i] = pieces;
+      // the start records of the decode CTAs whose first unit c W falls in [unit, u1)
+      const int4 r0 = make_int4(i, unit, u1, b);
+      const int4 r1 = make_int4(ctx_r, s0 + r, 0, 0);
+      for (int c = ceil_div(unit, W); c * W < u1; ++c) {
+        plan.cta_rec[2 * c] = r0;
+        plan.cta_rec[2 * c + 1] = r1;
+      }
+      slot += pieces;
+      unit = u1;
+    }
+  }
+  for (int j = 0; j < v.c; ++j) {
+    if (ex.c + j < max_tiles) {
+      plan.pf_seq[ex.c + j] = b;
+      plan.pf_tile[ex.c + j] = j;
+    }
+  }
+  if (threadIdx.x == 0) {
+    plan.dec_unit[n_dec] = U;
+    plan.header[0] = n_dec;
+    plan.header[1] = U;
+    plan.header[2] = W;
+    plan.header[3] = n_tiles;
+    plan.header[4] = ptot.a;
+    plan.header[5] = pn;
+  }
+}
+
 template <int D, int G>
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   using C = DecodeCfg<D, G>;
@@ -491,10 +651,16 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
   // no prefill kernel is launched (its idle CTAs would hold the SMs between the planner and
   // the decode), and the rows of such a span become decode entries.
   const bool rows_in_decode = a.num_tokens <= a.num_seqs;
-  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
-                             static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps,
-                             a.decode_ctas, tile_q,
-                             a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.err);
+  // up to kPlanThreads sequences: one thread each, the workspace written at the end (and, with
+  // plan_early, the arithmetic done before the wait on the previous kernel)
+  cudaError_t e =
+      a.num_seqs <= kPlanThreads
+          ? launch_pdl(plan_kernel_small, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
+                       static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps, a.decode_ctas,
+                       tile_q, a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.plan_early ? 1 : 0, a.err)
+          : launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
+                       static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps, a.decode_ctas,
+                       tile_q, a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.err);
   record_kernel_event(PKV_KERNEL_PLAN, true, stream);
   if (e != cudaSuccess) return e;
   auto prefill = [&](cudaStream_t s, bool pdl) -> cudaError_t {

@@ -129,6 +129,7 @@ struct AttnArgs {
   int prefill_kernel;  // 1 mma.sync tiles, 2 tcgen05 tiles (resolved from the process setting)
   int overlap;         // 1: prefill tiles run beside the decode on a second stream (SMs split)
   int fault;           // test-only fault injection (pkv_set_fault_injection); 0 in normal use
+  int plan_early;      // 1: the planner computes before waiting on the previous kernel (PKV_ATTN_PLAN_EARLY)
   cudaStream_t side_stream;  // the caller's second stream for the prefill beside the decode, or null
   cudaEvent_t fork_event, join_event;  // (with it) the caller's events ordering that stream
   Plan plan;

@@ -158,16 +158,18 @@ def alloc_workspace(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, m
 
 
 _OVERLAP = {None: 0, True: 1, False: 2}
+PLAN_EARLY = 1  # PKV_ATTN_PLAN_EARLY
 
 
-def _options(options):
-    """A pkv_attention_options from a dict: decode_kernel ('auto' | 'simt' | 'tensor'),
-    prefill_kernel ('auto' | 'mma' | 'tcgen05'), overlap (None | True | False), decode_ctas (int),
-    side_stream (torch.cuda.Stream) with fork_event and join_event (torch.cuda.Event)."""
-    if options is None:
-        return None
-    unknown = set(options) - {"decode_kernel", "prefill_kernel", "overlap", "decode_ctas", "side_stream",
-                              "fork_event", "join_event"}
+def attention_options(options):
+    """A pkv_attention_options from a dict (build it once and pass it to every call):
+    decode_kernel ('auto' | 'simt' | 'tensor'), prefill_kernel ('auto' | 'mma' | 'tcgen05'),
+    overlap (None | True | False), decode_ctas (int), plan_early (bool: PKV_ATTN_PLAN_EARLY, see include/pkv.h), side_stream (torch.cuda.Stream)
+    with fork_event and join_event (torch.cuda.Event)."""
+    if options is None or isinstance(options, _lib.AttentionOptions):
+        return options  # (a struct built earlier is passed through: no per-call marshalling)
+    unknown = set(options) - {"decode_kernel", "prefill_kernel", "overlap", "decode_ctas", "plan_early",
+                              "side_stream", "fork_event", "join_event"}
     if unknown:
         raise ValueError(f"unknown options {sorted(unknown)}")
     opt = _lib.AttentionOptions()
@@ -176,6 +178,7 @@ def _options(options):
     opt.prefill_kernel = PREFILL_KERNELS[options.get("prefill_kernel", "auto")]
     opt.overlap = _OVERLAP[options.get("overlap", None)]
     opt.decode_ctas = int(options.get("decode_ctas", 0))
+    opt.flags = PLAN_EARLY if options.get("plan_early", False) else 0
     side = options.get("side_stream")
     if side is not None:
         fork, join = options.get("fork_event"), options.get("join_event")
@@ -191,7 +194,8 @@ def _options(options):
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, out=None,
                     workspace=None, max_blocks_per_seq=None, stream=None, options=None):
     """Paged GQA over a ragged prefill/decode batch (``pkv_paged_attention``, or with per-call
-    ``options`` -- a dict, see ``_options`` -- ``pkv_paged_attention_ex``).  Returns out."""
+    ``options`` -- a dict or a struct from ``attention_options`` -- ``pkv_paged_attention_ex``).
+    Returns out."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
@@ -217,7 +221,7 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, query_start
     _need(out, "out", torch.bfloat16, 3)
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")
-    opt = _options(options)
+    opt = attention_options(options)
     if workspace is None:
         workspace = alloc_workspace(T, B, hq, hkv, d, mb, device=q.device,
                                     decode_ctas=opt.decode_ctas if opt is not None else 0)

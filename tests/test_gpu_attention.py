@@ -481,6 +481,44 @@ def test_per_call_options_equal_the_process_settings(opts, overlap_setting):
     assert_close(got.float().cpu().numpy(), ref, f"options {opts}")
 
 
+@pytest.mark.parametrize("index", [3, 5])
+def test_early_planner_gives_the_same_plan(index):
+    # PKV_ATTN_PLAN_EARLY after the step's kv_append (the use it is meant for): the same plan,
+    # so the same kernels and bit-identical rows, and the oracle's result
+    bt = W.config(index)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
+                                     bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    outs = []
+    for opts in (None, {"plan_early": True}):
+        d = Dev(bt)
+        d.append()
+        outs.append(ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                                        options=opts))
+        torch.cuda.synchronize()
+        assert ops.get_device_error() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert_close(outs[1].float().cpu().numpy(), ref, "early planner")
+
+
+@pytest.mark.parametrize("plan_early", [False, True])
+def test_more_sequences_than_planner_threads(plan_early):
+    # 1500 one-row spans: the multi-pass planner (the early flag is ignored there)
+    rng = np.random.default_rng(11)
+    ctx = rng.integers(1, 200, size=1500)
+    pages = int(sum(-(-int(c) // 16) for c in ctx))
+    bt = W.make_batch(ctx, [1] * 1500, 4, 2, 64, pages + 4, seed=11)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
+                                     bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    d = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
+    got = ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                              options={"plan_early": plan_early})
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    assert_close(got.float().cpu().numpy(), ref, "1500 sequences")
+
+
 def test_caller_side_stream_gives_the_same_result():
     # the prefill beside the decode on the caller's own second stream and events
     bt, q_rot, kc, vc, ref = config_with_oracle(5)
