@@ -91,27 +91,37 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, un
 // writer publishes its state (fence) before counting itself in dec_count[i]; the CTA that
 // counts last reads every state through L2 and writes the bf16 row.  No thread waits for
 // another CTA, so there is no inter-CTA spin.
+// `chunks` and `slot0` are the entry's dec_chunks[i] and dec_slot[i].  The (m, l) of the first
+// kMergeCached pieces are read once, in one batch, and kept in registers.
+constexpr int kMergeCached = 8;
 template <int D>
-__device__ void finish_split(const DecodeParams& p, int i, int64_t tq, volatile int* last_flag) {
+__device__ void finish_split(const DecodeParams& p, int i, int64_t tq, int chunks, int slot0,
+                             volatile int* last_flag) {
   __threadfence();
   named_bar_sync(1, kDecodeWarps * 32);
-  const int chunks = p.plan.dec_chunks[i];
   if (threadIdx.x == 0) *last_flag = atomicAdd(&p.plan.dec_count[i], 1) == chunks - 1;
   named_bar_sync(1, kDecodeWarps * 32);
   if (*last_flag) {
     __threadfence();
-    const int slot0 = p.plan.dec_slot[i];
     for (int item = threadIdx.x; item < p.hq * (D / 4); item += kDecodeWarps * 32) {
       const int h = item / (D / 4);
       const int d0 = (item - h * (D / 4)) * 4;
+      float2 mlc[kMergeCached];
+#pragma unroll
+      for (int k = 0; k < kMergeCached; ++k)
+        if (k < chunks)
+          mlc[k] = __ldcg(reinterpret_cast<const float2*>(p.plan.part_ml +
+                                                          (static_cast<int64_t>(slot0 + k) * p.hq + h) * 2));
       float M = -__int_as_float(0x7f800000);
-      for (int k = 0; k < chunks; ++k)
+#pragma unroll
+      for (int k = 0; k < kMergeCached; ++k)
+        if (k < chunks) M = fmaxf(M, mlc[k].x);
+      for (int k = kMergeCached; k < chunks; ++k)
         M = fmaxf(M, __ldcg(p.plan.part_ml + (static_cast<int64_t>(slot0 + k) * p.hq + h) * 2));
       float num[4] = {0.f, 0.f, 0.f, 0.f};
       float den = 0.f;
-      for (int k = 0; k < chunks; ++k) {
+      auto add_piece = [&](int k, float2 ml) {
         const int64_t sh = static_cast<int64_t>(slot0 + k) * p.hq + h;
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.plan.part_ml + sh * 2));
         const float w = fast_exp2(ml.x - M);
         den = fmaf(w, ml.y, den);
         const float4 a = __ldcg(reinterpret_cast<const float4*>(p.plan.part_acc + sh * D + d0));
@@ -119,7 +129,13 @@ __device__ void finish_split(const DecodeParams& p, int i, int64_t tq, volatile 
         num[1] = fmaf(w, a.y, num[1]);
         num[2] = fmaf(w, a.z, num[2]);
         num[3] = fmaf(w, a.w, num[3]);
-      }
+      };
+#pragma unroll
+      for (int k = 0; k < kMergeCached; ++k)
+        if (k < chunks) add_piece(k, mlc[k]);
+      for (int k = kMergeCached; k < chunks; ++k)
+        add_piece(k, __ldcg(reinterpret_cast<const float2*>(p.plan.part_ml +
+                                                            (static_cast<int64_t>(slot0 + k) * p.hq + h) * 2)));
       const float inv = 1.f / den;
       uint2 o;
       o.x = pack_bf16x2(num[0] * inv, num[1] * inv);
@@ -469,7 +485,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
         }
       }
     }
-    if (p.plan.dec_chunks[i] > 1) finish_split<D>(p, i, tq, last_flag);
+    if (p.plan.dec_chunks[i] > 1) finish_split<D>(p, i, tq, p.plan.dec_chunks[i], p.plan.dec_slot[i], last_flag);
     seg_start = true;
     ++i;
   }

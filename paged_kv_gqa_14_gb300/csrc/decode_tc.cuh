@@ -246,6 +246,25 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   bool ok = true;
   int it = 0;
   const uint32_t stage_base = smem_u32(stages);
+  const bool hv = gr < G;
+  // The next segment's entry (i + 1), when it starts inside this CTA's range, is read while
+  // this segment runs: its unit end, context and query row at this segment's start, its Q
+  // fragments after this segment's first unit.  A segment boundary then waits on no global
+  // read, while the producer's ring stays full.
+  int nx_unext = 0, nx_ctx = 0;
+  int64_t nx_tq = 0;
+  uint32_t nx_qb[KS][2];
+  bool nx_pending = false, nx_have_q = false;
+  int chunks = 1, slot0 = 0;  // the current entry's split pieces and first split slot
+  auto load_q = [&](int64_t row_tq, uint32_t (&dst)[KS][2]) {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        p.q + row_tq * p.q_st + static_cast<int64_t>(h * G + (hv ? gr : 0)) * p.q_sh);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      dst[kk][0] = hv ? qrow[kk * 8 + tig] : 0u;
+      dst[kk][1] = hv ? qrow[kk * 8 + 4 + tig] : 0u;
+    }
+  };
   for (int u = ubeg; u < uend; ++u, ++it) {
     if (seg_start) {
       if (i == i_first) {
@@ -253,20 +272,31 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
         unext = rec0.z;
         ctx = rec1.x;
         tq = rec1.y;
+        load_q(tq, qb);
       } else {
-        ustart = dec_unit[i];
-        unext = dec_unit[i + 1];
-        ctx = p.plan.dec_ctx[i];
-        tq = p.plan.dec_tq[i];
+        ustart = unext;  // entries are consecutive: this one starts where the last one ended
+        unext = nx_unext;
+        ctx = nx_ctx;
+        tq = nx_tq;
+        if (nx_have_q) {
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            qb[kk][0] = nx_qb[kk][0];
+            qb[kk][1] = nx_qb[kk][1];
+          }
+        } else {
+          load_q(tq, qb);
+        }
       }
       npages = ceil_div(ctx, 16);
-      const bool hv = gr < G;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          p.q + tq * p.q_st + static_cast<int64_t>(h * G + (hv ? gr : 0)) * p.q_sh);
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        qb[kk][0] = hv ? qrow[kk * 8 + tig] : 0u;
-        qb[kk][1] = hv ? qrow[kk * 8 + 4 + tig] : 0u;
+      chunks = p.plan.dec_chunks[i];
+      slot0 = p.plan.dec_slot[i];
+      nx_pending = unext < uend;
+      nx_have_q = false;
+      if (nx_pending) {
+        nx_unext = dec_unit[i + 2];
+        nx_ctx = p.plan.dec_ctx[i + 1];
+        nx_tq = p.plan.dec_tq[i + 1];
       }
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
@@ -354,6 +384,10 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+    if (nx_pending && !nx_have_q) {  // (the next entry's query row has arrived by now)
+      load_q(nx_tq, nx_qb);
+      nx_have_q = true;
+    }
 
     const bool seg_end = (u + 1 == unext) || (u + 1 == uend);
     if (!seg_end) continue;
@@ -383,8 +417,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     }
     named_bar_sync(1, kDecodeWarps * 32);
     {
-      const int chunks = p.plan.dec_chunks[i];
-      const int slot = p.plan.dec_slot[i] + (static_cast<int>(blockIdx.x) - ustart / W);
+      const int slot = slot0 + (static_cast<int>(blockIdx.x) - ustart / W);
       const int tid = threadIdx.x;  // 0..255
       for (int item = tid; item < hkv * G * (D / 4); item += kDecodeWarps * 32) {
         const int hh = item / (G * (D / 4));
@@ -417,7 +450,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
       }
     }
     named_bar_sync(1, kDecodeWarps * 32);
-    if (p.plan.dec_chunks[i] > 1) finish_split<D>(p, i, tq, last_flag);
+    if (chunks > 1) finish_split<D>(p, i, tq, chunks, slot0, last_flag);
     seg_start = true;
     ++i;
   }
