@@ -69,6 +69,18 @@ def test_append_random_shapes(seed):
     _check_append(bt, Dev(bt))
 
 
+@pytest.mark.parametrize("d,hq,hkv", [(128, 16, 8), (64, 14, 2), (128, 28, 4)])
+def test_append_large_step_matches_oracle(d, hq, hkv):
+    # 3000 new tokens in one step (about 20 per SM), every 97th a padding token with slot -1
+    rng = np.random.default_rng(d + hq)
+    ctx = rng.integers(1, 40, size=3000)
+    pages = int(sum(-(-int(c) // 16) for c in ctx))
+    bt = W.make_batch(ctx, [1] * 3000, hq, hkv, d, pages + 2, seed=d + hq)
+    bt.slot_mapping = bt.slot_mapping.copy()
+    bt.slot_mapping[::97] = -1
+    _check_append(bt, Dev(bt))
+
+
 def test_append_skips_negative_slots_and_flags_out_of_range():
     bt = W.make_batch([5, 20, 33, 2], [1, 1, 1, 1], 8, 4, 128, 12, seed=3)
     slots = bt.slot_mapping.copy()
