@@ -543,19 +543,35 @@ def run_gpu(args, rank, world, local_rank):
     # staged in one pinned host buffer, go up in one copy; the result comes back to pinned host
     from paged_kv_gqa_14_gb300.staging import StepStaging
 
-    kernel_copy = args.e2e_copy == "kernel"
-    stg = StepStaging(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
-                      bt.block_tables.shape[1], device=dev, kernel_copy=kernel_copy)
+    # auto: steps timed back to back overlap the copies with the steps, where the copy engines
+    # win (no SMs taken from the step); a step timed alone waits for its copies, where the copy
+    # kernel's lower start-up wins (measured on GB300)
+    e2e_copy = args.e2e_copy if args.e2e_copy != "auto" else ("kernel" if flush else "engine")
+    kernel_copy = e2e_copy == "kernel"
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)  # noqa: E731
-    stg.host.q.copy_(bf(bt.q))
-    stg.host.k.copy_(bf(bt.k))
-    stg.host.v.copy_(bf(bt.v))
-    stg.host.positions.copy_(torch.from_numpy(bt.positions))
-    stg.host.slot_mapping.copy_(torch.from_numpy(bt.slot_mapping))
-    stg.host.block_tables.copy_(torch.from_numpy(bt.block_tables))
-    stg.host.context_lens.copy_(torch.from_numpy(bt.context_lens))
-    stg.host.query_start_loc.copy_(torch.from_numpy(bt.query_start_loc))
+
+    def staged():
+        st = StepStaging(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
+                         bt.block_tables.shape[1], device=dev, kernel_copy=kernel_copy)
+        st.host.q.copy_(bf(bt.q))
+        st.host.k.copy_(bf(bt.k))
+        st.host.v.copy_(bf(bt.v))
+        st.host.positions.copy_(torch.from_numpy(bt.positions))
+        st.host.slot_mapping.copy_(torch.from_numpy(bt.slot_mapping))
+        st.host.block_tables.copy_(torch.from_numpy(bt.block_tables))
+        st.host.context_lens.copy_(torch.from_numpy(bt.context_lens))
+        st.host.query_start_loc.copy_(torch.from_numpy(bt.query_start_loc))
+        return st
+
+    stg = staged()
     sd = stg.dev
+    # (back to back) the next step's inputs go up on their own stream into a second staging
+    # buffer while this step runs: every step's inputs still cross the link inside the timed
+    # region, one step ahead, as its result crosses back one step behind
+    stgs = [stg, staged()] if not flush else [stg]
+    h2d_stream = torch.cuda.Stream(device=dev) if not flush else stream
+    in_ready = [torch.cuda.Event(), torch.cuda.Event()]  # the step's inputs are on the device
+    in_free = [torch.cuda.Event(), torch.cuda.Event()]   # the step that read them has finished
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = stg.nbytes
     d2h = host_out.numel() * host_out.element_size()
@@ -570,7 +586,11 @@ def run_gpu(args, rank, world, local_rank):
     out_free = [torch.cuda.Event(), torch.cuda.Event()]   # outs[j] is back on the host
     for j in range(2):
         out_free[j].record(stream)
+        in_free[j].record(stream)
     e2e_no = [0]
+    if not flush:  # the first step's inputs
+        stgs[0].upload(h2d_stream)
+        in_ready[0].record(h2d_stream)
 
     def e2e_step():
         if flush:  # one step alone: upload, step, copy back, all on the step's stream
@@ -585,11 +605,17 @@ def run_gpu(args, rank, world, local_rank):
             return
         j = e2e_no[0] & 1
         e2e_no[0] += 1
-        stg.upload(stream)
-        ops.kv_append(sd.q, sd.k, sd.v, sd.positions, sd.slot_mapping, kc, vc, bt.rope_theta)
+        nj = 1 - j
+        h2d_stream.wait_event(in_free[nj])  # the next step's staging buffer, once free
+        stgs[nj].upload(h2d_stream)
+        in_ready[nj].record(h2d_stream)
+        stream.wait_event(in_ready[j])
+        sdj = stgs[j].dev
+        ops.kv_append(sdj.q, sdj.k, sdj.v, sdj.positions, sdj.slot_mapping, kc, vc, bt.rope_theta)
         stream.wait_event(out_free[j])
-        ops.paged_attention(sd.q, kc, vc, sd.block_tables, sd.context_lens, sd.query_start_loc, bt.scale,
+        ops.paged_attention(sdj.q, kc, vc, sdj.block_tables, sdj.context_lens, sdj.query_start_loc, bt.scale,
                             out=outs[j], workspace=ws, options=attn_opts)
+        in_free[j].record(stream)
         out_ready[j].record(stream)
         d2h_stream.wait_event(out_ready[j])
         if kernel_copy:
@@ -692,10 +718,13 @@ def run_gpu(args, rank, world, local_rank):
             "ms_per_step": round(e2e_ms, 5),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "copy": args.e2e_copy,
+            "copy": e2e_copy,
             "pipeline": ("each step alone: upload, step, result copied back, on one stream" if flush else
-                         "each step's result copied back on a second stream while the next step uploads and "
-                         "runs (double-buffered out); the timed region ends with the last result on the host"),
+                         "each step's inputs uploaded on a third stream one step ahead, into the other of two "
+                         "staging buffers, while the step before runs; its result copied back on a second "
+                         "stream while the next step runs (double-buffered out); every step's inputs and "
+                         "result cross the link inside the timed region, which ends with the last result on "
+                         "the host"),
         },
         # kv_append, planner, decode split-K (+ merge), and the prefill tiles when a span can
         # hold two or more tokens
@@ -781,9 +810,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--e2e-copy", choices=["engine", "kernel"], default="kernel",
+    ap.add_argument("--e2e-copy", choices=["auto", "engine", "kernel"], default="auto",
                     help="end-to-end leg: move the staged inputs and the output with the copy engines "
-                         "(cudaMemcpyAsync) or with a copy kernel reading/writing pinned host memory")
+                         "(cudaMemcpyAsync) or with a copy kernel reading/writing pinned host memory "
+                         "(auto: engines when steps run back to back, the kernel when each runs alone)")
     ap.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32, 64, 128],
                     help="tokens per pool block (the workload keeps its pool size in tokens)")
     ap.add_argument("--seqs", type=int, default=0, help="only the first N sequences (small profiling case)")
