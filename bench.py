@@ -609,10 +609,12 @@ def run_gpu(args, rank, world, local_rank):
         h2d_stream.wait_event(in_free[nj])  # the next step's staging buffer, once free
         stgs[nj].upload(h2d_stream)
         in_ready[nj].record(h2d_stream)
+        # both waits before the append, so that nothing sits between the append and the
+        # attention call (the planner overlaps the append only when they are adjacent)
+        stream.wait_event(out_free[j])
         stream.wait_event(in_ready[j])
         sdj = stgs[j].dev
         ops.kv_append(sdj.q, sdj.k, sdj.v, sdj.positions, sdj.slot_mapping, kc, vc, bt.rope_theta)
-        stream.wait_event(out_free[j])
         ops.paged_attention(sdj.q, kc, vc, sdj.block_tables, sdj.context_lens, sdj.query_start_loc, bt.scale,
                             out=outs[j], workspace=ws, options=attn_opts)
         in_free[j].record(stream)
