@@ -91,59 +91,96 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, un
 // writer publishes its state (fence) before counting itself in dec_count[i]; the CTA that
 // counts last reads every state through L2 and writes the bf16 row.  No thread waits for
 // another CTA, so there is no inter-CTA spin.
-// `chunks` and `slot0` are the entry's dec_chunks[i] and dec_slot[i].  The (m, l) of the first
-// kMergeCached pieces are read once, in one batch, and kept in registers.
-constexpr int kMergeCached = 8;
+// `chunks` and `slot0` are the entry's dec_chunks[i] and dec_slot[i].  A thread merges
+// kMergeItems float4 items (head, 4 dims) at a time and reads the pieces in groups of
+// kMergeGroup: the (m, l) and acc loads of a whole group and of all its items are issued
+// together, so an entry of up to kMergeGroup pieces costs one round trip to L2 per pass.
+// Groups after the first are folded in with a running maximum (the online form of the same
+// sum); with at most kMergeGroup pieces the sum is the plain one above, in piece order.
+constexpr int kMergeItems = 1;
+constexpr int kMergeGroup = 4;
 template <int D>
 __device__ void finish_split(const DecodeParams& p, int i, int64_t tq, int chunks, int slot0,
                              volatile int* last_flag) {
+  constexpr int kThreads = kDecodeWarps * 32;
+  constexpr int kQ = D / 4;
   __threadfence();
-  named_bar_sync(1, kDecodeWarps * 32);
+  named_bar_sync(1, kThreads);
   if (threadIdx.x == 0) *last_flag = atomicAdd(&p.plan.dec_count[i], 1) == chunks - 1;
-  named_bar_sync(1, kDecodeWarps * 32);
+  named_bar_sync(1, kThreads);
   if (*last_flag) {
     __threadfence();
-    for (int item = threadIdx.x; item < p.hq * (D / 4); item += kDecodeWarps * 32) {
-      const int h = item / (D / 4);
-      const int d0 = (item - h * (D / 4)) * 4;
-      float2 mlc[kMergeCached];
+    const int hq = p.hq;
+    const int nitems = hq * kQ;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    for (int base = threadIdx.x; base < nitems; base += kMergeItems * kThreads) {
+      float M[kMergeItems], den[kMergeItems];
+      float4 num[kMergeItems];
 #pragma unroll
-      for (int k = 0; k < kMergeCached; ++k)
-        if (k < chunks)
-          mlc[k] = __ldcg(reinterpret_cast<const float2*>(p.plan.part_ml +
-                                                          (static_cast<int64_t>(slot0 + k) * p.hq + h) * 2));
-      float M = -__int_as_float(0x7f800000);
+      for (int j = 0; j < kMergeItems; ++j) {
+        M[j] = NEG_INF;
+        den[j] = 0.f;
+        num[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int k0 = 0; k0 < chunks; k0 += kMergeGroup) {
+        float2 ml[kMergeGroup][kMergeItems];
+        float4 a[kMergeGroup][kMergeItems];
 #pragma unroll
-      for (int k = 0; k < kMergeCached; ++k)
-        if (k < chunks) M = fmaxf(M, mlc[k].x);
-      for (int k = kMergeCached; k < chunks; ++k)
-        M = fmaxf(M, __ldcg(p.plan.part_ml + (static_cast<int64_t>(slot0 + k) * p.hq + h) * 2));
-      float num[4] = {0.f, 0.f, 0.f, 0.f};
-      float den = 0.f;
-      auto add_piece = [&](int k, float2 ml) {
-        const int64_t sh = static_cast<int64_t>(slot0 + k) * p.hq + h;
-        const float w = fast_exp2(ml.x - M);
-        den = fmaf(w, ml.y, den);
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.plan.part_acc + sh * D + d0));
-        num[0] = fmaf(w, a.x, num[0]);
-        num[1] = fmaf(w, a.y, num[1]);
-        num[2] = fmaf(w, a.z, num[2]);
-        num[3] = fmaf(w, a.w, num[3]);
-      };
+        for (int kk = 0; kk < kMergeGroup; ++kk) {
 #pragma unroll
-      for (int k = 0; k < kMergeCached; ++k)
-        if (k < chunks) add_piece(k, mlc[k]);
-      for (int k = kMergeCached; k < chunks; ++k)
-        add_piece(k, __ldcg(reinterpret_cast<const float2*>(p.plan.part_ml +
-                                                            (static_cast<int64_t>(slot0 + k) * p.hq + h) * 2)));
-      const float inv = 1.f / den;
-      uint2 o;
-      o.x = pack_bf16x2(num[0] * inv, num[1] * inv);
-      o.y = pack_bf16x2(num[2] * inv, num[3] * inv);
-      *reinterpret_cast<uint2*>(p.out + tq * p.o_st + static_cast<int64_t>(h) * p.o_sh + d0) = o;
+          for (int j = 0; j < kMergeItems; ++j) {
+            const int item = base + j * kThreads;
+            const int h = item / kQ;
+            const int64_t sh = static_cast<int64_t>(slot0 + k0 + kk) * hq + h;
+            if (k0 + kk < chunks && item < nitems) {
+              ml[kk][j] = __ldcg(reinterpret_cast<const float2*>(p.plan.part_ml + sh * 2));
+              a[kk][j] = __ldcg(reinterpret_cast<const float4*>(p.plan.part_acc + sh * D) + (item - h * kQ));
+            } else {
+              ml[kk][j] = make_float2(NEG_INF, 0.f);
+              a[kk][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kMergeItems; ++j) {
+          float Mn = M[j];
+#pragma unroll
+          for (int kk = 0; kk < kMergeGroup; ++kk) Mn = fmaxf(Mn, ml[kk][j].x);
+          if (Mn == NEG_INF) continue;  // an item past the end (every piece holds a key)
+          const float c = fast_exp2(M[j] - Mn);  // 0 on the first group
+          den[j] *= c;
+          num[j].x *= c;
+          num[j].y *= c;
+          num[j].z *= c;
+          num[j].w *= c;
+#pragma unroll
+          for (int kk = 0; kk < kMergeGroup; ++kk) {
+            const float w = fast_exp2(ml[kk][j].x - Mn);  // 0 for a piece past the entry
+            den[j] = fmaf(w, ml[kk][j].y, den[j]);
+            num[j].x = fmaf(w, a[kk][j].x, num[j].x);
+            num[j].y = fmaf(w, a[kk][j].y, num[j].y);
+            num[j].z = fmaf(w, a[kk][j].z, num[j].z);
+            num[j].w = fmaf(w, a[kk][j].w, num[j].w);
+          }
+          M[j] = Mn;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kMergeItems; ++j) {
+        const int item = base + j * kThreads;
+        if (item < nitems) {
+          const int h = item / kQ;
+          const int d0 = (item - h * kQ) * 4;
+          const float inv = 1.f / den[j];
+          uint2 o;
+          o.x = pack_bf16x2(num[j].x * inv, num[j].y * inv);
+          o.y = pack_bf16x2(num[j].z * inv, num[j].w * inv);
+          *reinterpret_cast<uint2*>(p.out + tq * p.o_st + static_cast<int64_t>(h) * p.o_sh + d0) = o;
+        }
+      }
     }
   }
-  named_bar_sync(1, kDecodeWarps * 32);  // last_flag is reused by the next segment
+  named_bar_sync(1, kThreads);  // last_flag is reused by the next segment
 }
 
 // Load this lane's DPL bf16 of one row and widen to fp32.

@@ -195,15 +195,19 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
       const int pg0 = (u - ustart) * pps;
       const int npg = min(pps, npages - pg0);
       const int s = it % STAGES;
-      if (it >= STAGES && !wait_or_abort(&empty[s], ((it / STAGES) - 1) & 1, p.err, abort_flag)) break;
       int blk = 0, blk2 = -1;
       const bool issue = lane_has_box && bp < npg;
       const int gp = pg0 + bp;
       if (issue) {
+        // the unit's block ids are requested before the wait for its stage, so their latency
+        // passes while the ring is full, and a freed stage is refilled at once; both reads are
+        // issued before either is checked
         const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
-        // both reads are issued before either is checked, so their latencies overlap
         blk = row[two_blocks ? 2 * gp : gp >> (sh >= 4 ? sh - 4 : 0)];
         if (two_blocks && gp * 16 + 8 < ctx) blk2 = row[2 * gp + 1];
+      }
+      if (it >= STAGES && !wait_or_abort(&empty[s], ((it / STAGES) - 1) & 1, p.err, abort_flag)) break;
+      if (issue) {
         if (blk < 0 || blk >= p.num_blocks) {
           raise_error(p.err, PKV_DEVERR_BLOCK_RANGE);
           blk = 0;
