@@ -418,8 +418,12 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     # the step's kv_append sits between the index tables' upload and the attention call, so the
-    # planner may do its arithmetic while the append runs (PKV_ATTN_PLAN_EARLY)
-    attn_opts = ops.attention_options({"plan_early": not args.no_plan_early})
+    # planner may do its arithmetic while the append runs (PKV_ATTN_PLAN_EARLY) and, for a batch
+    # large enough that it pays, the decode may copy the pages that hold no new key meanwhile
+    # (PKV_ATTN_STREAM_EARLY)
+    stream_early = not (args.no_plan_early or args.no_stream_early) and ops.stream_early_pays(
+        bt.num_seqs, bt.block_tables.shape[1], bt.block_size)
+    attn_opts = ops.attention_options({"plan_early": not args.no_plan_early, "stream_early": stream_early})
 
     def step():
         ops.kv_append(q, k, v, pos, slots, kc, vc, bt.rope_theta)
@@ -675,6 +679,7 @@ def run_gpu(args, rank, world, local_rank):
             "prefill_kernel": args.prefill_kernel,
             "prefill_beside_decode": not args.no_overlap,
             "plan_early": not args.no_plan_early,
+            "stream_early": stream_early,
             "l2": ("L2 flushed between timed steps (unique KV per step %.1f MB < 2 x 129 MB): a %d MiB "
                    "scratch write before each step, each step timed alone with CUDA events"
                    % (kv_u / 1e6, FLUSH_BYTES >> 20)) if flush else
@@ -823,6 +828,9 @@ def main():
     ap.add_argument("--prefill-kernel", choices=["auto", "mma", "tcgen05"], default="auto")
     ap.add_argument("--no-plan-early", action="store_true",
                     help="plan after the append has finished (default: the planner computes while it runs)")
+    ap.add_argument("--no-stream-early", action="store_true",
+                    help="the decode reads the plan after the append has finished (default: it copies "
+                         "the pages without new keys while the append runs)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="prefill tiles before the decode on one stream (default: beside it, SMs split)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -241,6 +241,20 @@ PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64
  *                   nor lets later work start before their writer has finished: the step's
  *                   pkv_kv_append qualifies (it waits for all earlier work before it lets later
  *                   work start).  Batches of more than 1024 sequences ignore the flag.
+ *                   PKV_ATTN_STREAM_EARLY (implies PKV_ATTN_PLAN_EARLY): besides, the planner
+ *                   writes the workspace as soon as the plan is known, and the tensor-core
+ *                   decode starts copying the pages that hold no key of this step's new tokens
+ *                   while that work may still be running; it reads q, and every page that may
+ *                   hold a new token's key, only once that work has finished.  Set it only when
+ *                   that work also writes nothing this call reads except q and the new tokens'
+ *                   slots of k_cache and v_cache (positions context - span .. context - 1 of each
+ *                   sequence), and starts later work only after all work before it has finished
+ *                   (so no kernel of an earlier call still reads the workspace): the step's
+ *                   pkv_kv_append qualifies.  Batches of more than 1024 sequences ignore it.
+ *                   The decode then learns that the plan is ready through a word the planner
+ *                   publishes, about one round trip to L2 later than through the planner's end:
+ *                   on a small, latency-bound batch that costs more than it hides (GB300: about
+ *                   +1 us for 32 sequences of up to 1152 keys, -2 us for 256 of up to 2048).
  *   side_stream, fork_event, join_event
  *                   all NULL: the library's own second stream for the prefill beside the
  *                   decode; else a caller-owned stream (cudaStream_t) and two caller-created
@@ -252,6 +266,7 @@ PKV_API int pkv_paged_attention(const void* q_dev, int64_t q_stride_token, int64
  * handles given give PKV_ERR_NULL.
  */
 #define PKV_ATTN_PLAN_EARLY 1
+#define PKV_ATTN_STREAM_EARLY 2
 typedef struct pkv_attention_options {
   uint32_t struct_size;
   int32_t decode_kernel;

@@ -323,7 +323,7 @@ int paged_attention_impl(const void* q, int64_t q_st, int64_t q_sh, const void* 
     if (opt->struct_size != sizeof(pkv_attention_options)) return PKV_ERR_SHAPE;
     if (opt->decode_kernel < 0 || opt->decode_kernel > 2 || opt->prefill_kernel < 0 || opt->prefill_kernel > 2 ||
         opt->overlap < 0 || opt->overlap > 2 || opt->decode_ctas < 0 || opt->decode_ctas > kMaxDecodeCtas ||
-        (opt->flags & ~PKV_ATTN_PLAN_EARLY) != 0)
+        (opt->flags & ~(PKV_ATTN_PLAN_EARLY | PKV_ATTN_STREAM_EARLY)) != 0)
       return PKV_ERR_SHAPE;
     const int given = (opt->side_stream != nullptr) + (opt->fork_event != nullptr) + (opt->join_event != nullptr);
     if (given != 0 && given != 3) return PKV_ERR_NULL;
@@ -381,7 +381,11 @@ int paged_attention_impl(const void* q, int64_t q_st, int64_t q_sh, const void* 
   a.prefill_kernel = (opt && opt->prefill_kernel) ? opt->prefill_kernel : prefill_kernel_choice();
   a.overlap = (opt && opt->overlap) ? (opt->overlap == 1 ? 1 : 0) : overlap_choice();
   a.fault = fault_injection_choice();
-  a.plan_early = (opt && (opt->flags & PKV_ATTN_PLAN_EARLY)) ? 1 : 0;
+  const int flags = opt ? opt->flags : 0;
+  // early streaming needs the one-CTA planner (up to kSmallPlanMaxSeqs sequences), which
+  // publishes the plan; it implies early planning
+  a.stream_early = (flags & PKV_ATTN_STREAM_EARLY) && num_seqs <= kSmallPlanMaxSeqs ? 1 : 0;
+  a.plan_early = (flags & (PKV_ATTN_PLAN_EARLY | PKV_ATTN_STREAM_EARLY)) ? 1 : 0;
   a.side_stream = opt ? static_cast<cudaStream_t>(opt->side_stream) : nullptr;
   a.fork_event = opt ? static_cast<cudaEvent_t>(opt->fork_event) : nullptr;
   a.join_event = opt ? static_cast<cudaEvent_t>(opt->join_event) : nullptr;

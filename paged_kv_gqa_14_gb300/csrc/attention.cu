@@ -106,6 +106,7 @@ bool make_pool_map(CUtensorMap* m, const void* base, int64_t num_blocks, int bs_
 namespace {
 
 constexpr int kPlanThreads = 1024;
+static_assert(kPlanThreads == kSmallPlanMaxSeqs, "the small planner takes one sequence per thread");
 
 struct Int3 {
   int a, b, c;
@@ -337,13 +338,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 // before this call does not write them) and only the workspace writes come after it, so the
 // planner's work overlaps that kernel (the step's kv_append).  Without `early` it waits
 // first, like plan_kernel.
+// With `stream` (which implies `early`) the workspace is written as soon as the plan is known,
+// and header[kPlanReadyWord] then tells the decode it may start streaming pages (cleared
+// before this kernel lets the decode launch, set after every other workspace write): 1 when
+// each decode entry's new keys all lie in its last 16-token page (every entry is a span of
+// one token), 2 when some entry is a row of a longer span.  The kernel still waits on the
+// previous kernel before it ends, so work that waits for its end waits for that kernel too.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel_small(const int32_t* __restrict__ qsl,
                                                                   const int32_t* __restrict__ ctxl,
                                                                   int num_seqs, int64_t num_tokens,
                                                                   int64_t max_ctx, int pps, int decode_ctas,
                                                                   int tile_q, Plan plan, int64_t max_tiles,
                                                                   SplitArgs split, int rows_in_decode, int early,
-                                                                  unsigned int* err) {
+                                                                  int stream, unsigned int* err) {
   __shared__ int sm[3 * 32];
   __shared__ unsigned long long pf_keytiles;  // 128-key tiles over all prefill q tiles (one kv head)
   __shared__ int pf_maxtile;                  // the most key tiles of one q tile
@@ -353,7 +360,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel_small(const int32_t*
     pf_maxtile = 0;
     best = ~0ull;
   }
-  if (early) {
+  if (stream) {
+    if (threadIdx.x == 0) {
+      plan.header[kPlanReadyWord] = 0;
+      __threadfence();
+    }
+    __syncthreads();
+    pdl_trigger();  // the decode may start; it reads nothing of the plan before the ready word
+  } else if (early) {
     pdl_trigger();  // the decode may start its prologue; it waits for this kernel's end
   } else {
     pdl_wait();  // the workspace may still be read by the previous call's kernels until now
@@ -447,7 +461,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel_small(const int32_t*
   Int3 ptot;
   const Int3 pex = block_scan3(pc, ptot, sm);
 
-  if (early) pdl_wait();  // from here on the workspace is written
+  // a decode entry that is one row of a longer span has new keys before its last page
+  const int long_rows = __syncthreads_or(v.a > 1);
+  if (early && !stream) pdl_wait();  // from here on the workspace is written
   {
     int unit = ex.b, slot = pex.a;
     for (int r = 0; r < v.a; ++r) {
@@ -488,6 +504,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel_small(const int32_t*
     plan.header[4] = ptot.a;
     plan.header[5] = pn;
   }
+  if (stream) {
+    __syncthreads();  // every thread's workspace writes are done
+    if (threadIdx.x == 0) {
+      __threadfence();
+      st_release_gpu(plan.header + kPlanReadyWord, long_rows ? 2 : 1);
+    }
+    pdl_wait();  // this kernel ends after the previous one
+  }
 }
 
 template <int D, int G>
@@ -515,6 +539,7 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   p.plan = a.plan;
   p.err = a.err;
   p.fault_no_copies = 0;
+  p.stream_early = 0;  // this kernel waits for the whole plan
   record_kernel_event(PKV_KERNEL_DECODE, false, stream);
   const cudaError_t e = launch_pdl(decode_splitk_kernel<D, G>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
                                    C::kSmemBytes, stream, p);
@@ -657,7 +682,8 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
       a.num_seqs <= kPlanThreads
           ? launch_pdl(plan_kernel_small, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
                        static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps, a.decode_ctas,
-                       tile_q, a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.plan_early ? 1 : 0, a.err)
+                       tile_q, a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.plan_early ? 1 : 0,
+                       a.stream_early ? 1 : 0, a.err)
           : launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
                        static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps, a.decode_ctas,
                        tile_q, a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.err);

@@ -44,6 +44,7 @@ struct DecodeParams {
   Plan plan;
   unsigned int* err;
   int fault_no_copies;  // test-only: the tensor-core decode's producer issues nothing
+  int stream_early;     // the planner publishes header[kPlanReadyWord] (tensor-core decode only)
 };
 
 template <int D, int G>

@@ -48,6 +48,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   p.plan = a.plan;
   p.err = a.err;
   p.fault_no_copies = a.fault == PKV_FAULT_DECODE_NO_COPIES;
+  p.stream_early = a.stream_early;
   record_kernel_event(PKV_KERNEL_DECODE, false, stream);
   const cudaError_t e = launch_pdl(decode_tc_kernel<D, G, BS>, dim3(a.decode_ctas), dim3((kDecodeWarps + 1) * 32),
                                    C::kSmemBytes, stream, P);

@@ -116,6 +116,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   uint64_t* empty = full + STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
   volatile int* last_flag = abort_flag + 2;
+  volatile int* stream_mode = abort_flag + 4;
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -132,7 +133,26 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmap_v)) : "memory");
   }
-  pdl_wait();  // the plan is written by the planner kernel
+  // The plan is written by the planner kernel.  Streaming early, the CTA reads it as soon as
+  // the planner has published it (mode 1 or 2, see the ready word); the producer then copies
+  // pages while the kernel before the planner may still run, and waits for that kernel only
+  // before the first page that may hold a new key (mode 1: an entry's last page; mode 2: any),
+  // and the consumers before they read q.  Mode 0: everything before this kernel has finished.
+  int mode = 0;
+  if (p.stream_early) {
+    if (threadIdx.x == 0) {
+      int v;
+      const long long t0 = clock64();
+      while ((v = ld_acquire_gpu(p.plan.header + kPlanReadyWord)) == 0 && clock64() - t0 < kPlanReadySpinClocks)
+        __nanosleep(64);
+      *stream_mode = v;  // still 0 at the limit: every thread waits for the planner's end instead
+    }
+    __syncthreads();
+    mode = *stream_mode;
+    if (mode == 0) pdl_wait();
+  } else {
+    pdl_wait();
+  }
   pdl_trigger();
   const int* hdr = p.plan.header;
   const int U = hdr[1];
@@ -183,6 +203,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
     constexpr int bmask = BS - 1;
     constexpr bool two_blocks = BS == 8;
     int it = 0;
+    bool waited = mode == 0;
     for (int u = ubeg; u < uend; ++u, ++it) {
       while (u >= unext) {
         ++i;
@@ -217,6 +238,10 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
           blk2 = 0;
         }
       }
+      if (!waited && (mode == 2 || pg0 + npg - 1 >= (ctx - 1) >> 4)) {
+        pdl_wait();  // this unit may hold a key written by the kernel before the planner
+        waited = true;
+      }
       // a last half page past the context is not loaded (8-token blocks)
       const bool tail_half = two_blocks && (pg0 + npg - 1) * 16 + 8 >= ctx;
       if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * (npg * page_bytes - (tail_half ? page_bytes / 2 : 0u)));
@@ -235,6 +260,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, 1)
   }
 
   // -------------------------------------------------------------------- consumer warps
+  if (mode != 0) pdl_wait();  // q is written by the kernel before the planner
   const int pw = warp / hkv;
   const int h = warp - pw * hkv;
   const int gr = lane >> 2, tig = lane & 3;

@@ -42,10 +42,16 @@ constexpr int kTensorDecodeMinGroup = 1;
 // header[3] number of prefill (seq, q-tile) work items         n_tiles
 // header[4] partial-result slots in use                        S
 // header[5] prefill CTAs that take work items                  P (the rest leave at once)
+// header[8] plan ready word (kPlanReadyWord), written only when the decode streams early:
+//           0 while the plan is being written, then 1 (new keys only in each decode entry's
+//           last 16-token page) or 2 (some entry has new keys before its last page)
 //
 // A decode work unit is one page group of one sequence: P = kDecodeWarps / Hkv
 // consecutive 16-token pages (kPageTokens), all kv heads.  Decode CTA c owns units [c W, (c+1) W) of
 // the concatenation of all decode sequences' units.
+constexpr int kPlanReadyWord = 8;
+constexpr int kSmallPlanMaxSeqs = 1024;
+constexpr long long kPlanReadySpinClocks = 1ll << 24;  // a decode CTA's wait for the ready word  // batches the one-CTA, one-thread-per-sequence planner takes
 struct Plan {
   int* header;      // [16]
   int* dec_seq;     // [B]      decode list: sequence id
@@ -130,6 +136,8 @@ struct AttnArgs {
   int overlap;         // 1: prefill tiles run beside the decode on a second stream (SMs split)
   int fault;           // test-only fault injection (pkv_set_fault_injection); 0 in normal use
   int plan_early;      // 1: the planner computes before waiting on the previous kernel (PKV_ATTN_PLAN_EARLY)
+  int stream_early;    // 1: the plan is published at once and the tensor-core decode streams the
+                       // pages without new keys before the previous kernel ends (PKV_ATTN_STREAM_EARLY)
   cudaStream_t side_stream;  // the caller's second stream for the prefill beside the decode, or null
   cudaEvent_t fork_event, join_event;  // (with it) the caller's events ordering that stream
   Plan plan;

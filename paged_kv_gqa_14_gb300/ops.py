@@ -159,17 +159,33 @@ def alloc_workspace(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, m
 
 _OVERLAP = {None: 0, True: 1, False: 2}
 PLAN_EARLY = 1  # PKV_ATTN_PLAN_EARLY
+STREAM_EARLY = 2  # PKV_ATTN_STREAM_EARLY
+
+
+STREAM_EARLY_MIN_KEYS = 1 << 17
+
+
+def stream_early_pays(num_seqs, max_blocks_per_seq, block_size):
+    """Whether PKV_ATTN_STREAM_EARLY is worth setting for a batch of this size: the decode then
+    reads the plan through a published word, one round trip to L2 later than through the
+    planner's end, which costs about 1 us on a batch that is latency-bound anyway and is repaid
+    once the pages a decode CTA can copy during the append dominate (append + attention step on
+    one GB300: 32 sequences of up to 1152 keys, L2 flushed, 20.1 -> 21.2 us; 256 of up to 2048,
+    156.2 -> 154.0 us; 50 of 8192, 133.9 -> 132.5 us).  The rule: at least STREAM_EARLY_MIN_KEYS
+    key slots in the block tables."""
+    return num_seqs * max_blocks_per_seq * block_size >= STREAM_EARLY_MIN_KEYS
 
 
 def attention_options(options):
     """A pkv_attention_options from a dict (build it once and pass it to every call):
     decode_kernel ('auto' | 'simt' | 'tensor'), prefill_kernel ('auto' | 'mma' | 'tcgen05'),
-    overlap (None | True | False), decode_ctas (int), plan_early (bool: PKV_ATTN_PLAN_EARLY, see include/pkv.h), side_stream (torch.cuda.Stream)
-    with fork_event and join_event (torch.cuda.Event)."""
+    overlap (None | True | False), decode_ctas (int), plan_early (bool: PKV_ATTN_PLAN_EARLY),
+    stream_early (bool: PKV_ATTN_STREAM_EARLY; both flags are defined in include/pkv.h),
+    side_stream (torch.cuda.Stream) with fork_event and join_event (torch.cuda.Event)."""
     if options is None or isinstance(options, _lib.AttentionOptions):
         return options  # (a struct built earlier is passed through: no per-call marshalling)
     unknown = set(options) - {"decode_kernel", "prefill_kernel", "overlap", "decode_ctas", "plan_early",
-                              "side_stream", "fork_event", "join_event"}
+                              "stream_early", "side_stream", "fork_event", "join_event"}
     if unknown:
         raise ValueError(f"unknown options {sorted(unknown)}")
     opt = _lib.AttentionOptions()
@@ -178,7 +194,8 @@ def attention_options(options):
     opt.prefill_kernel = PREFILL_KERNELS[options.get("prefill_kernel", "auto")]
     opt.overlap = _OVERLAP[options.get("overlap", None)]
     opt.decode_ctas = int(options.get("decode_ctas", 0))
-    opt.flags = PLAN_EARLY if options.get("plan_early", False) else 0
+    opt.flags = (PLAN_EARLY if options.get("plan_early", False) else 0) | (
+        STREAM_EARLY if options.get("stream_early", False) else 0)
     side = options.get("side_stream")
     if side is not None:
         fork, join = options.get("fork_event"), options.get("join_event")

@@ -166,7 +166,7 @@ def test_attention_options_are_validated_on_the_host(lib):
     opt.struct_size = ctypes.sizeof(_lib.AttentionOptions) + 4  # another layout
     assert lib.pkv_paged_attention_ex(*_attn_ex_args(x, ctypes.byref(opt))) == 2  # PKV_ERR_SHAPE
     for field, value in [("decode_kernel", 3), ("prefill_kernel", -1), ("overlap", 3), ("decode_ctas", -1),
-                         ("decode_ctas", (1 << 16) + 1), ("flags", 2), ("flags", -1)]:
+                         ("decode_ctas", (1 << 16) + 1), ("flags", 4), ("flags", -1)]:
         opt = _lib.AttentionOptions()
         opt.struct_size = ctypes.sizeof(_lib.AttentionOptions)
         setattr(opt, field, value)

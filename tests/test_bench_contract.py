@@ -96,3 +96,25 @@ def test_traffic_record_is_read_back_only_for_the_same_sources(tmp_path, monkeyp
     assert bench.kernel_traffic("decode", "other") is None
     monkeypatch.setattr(bench, "source_sha256", lambda: "changed")
     assert bench.kernel_traffic("decode", "w3") is None
+
+
+@pytest.mark.parametrize("index", [1, 2])
+def test_early_streaming_rule_small_batches(index):
+    # PKV_ATTN_STREAM_EARLY is set for batches whose block tables hold at least 2^17 key slots:
+    # not for the two small workloads, at any block size (the rule counts tokens, not blocks)
+    from paged_kv_gqa_14_gb300 import ops
+    from paged_kv_gqa_14_gb300 import workloads as W
+
+    for bs in (8, 16, 128):
+        bt = W.config(index, poison=False, block_size=bs)
+        assert not ops.stream_early_pays(bt.num_seqs, bt.block_tables.shape[1], bt.block_size)
+
+
+def test_early_streaming_rule_large_batches():
+    # the three large workloads (sequences x longest context): 256 x 2048, 50 x 8192, 204 x 2048
+    from paged_kv_gqa_14_gb300 import ops
+
+    for seqs, keys in [(256, 2048), (50, 8192), (204, 2048)]:
+        for bs in (8, 16, 128):
+            assert ops.stream_early_pays(seqs, keys // bs, bs)
+    assert ops.stream_early_pays(1, 1 << 13, 16) and not ops.stream_early_pays(1, (1 << 13) - 1, 16)

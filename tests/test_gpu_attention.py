@@ -501,9 +501,89 @@ def test_early_planner_gives_the_same_plan(index):
     assert_close(outs[1].float().cpu().numpy(), ref, "early planner")
 
 
-@pytest.mark.parametrize("plan_early", [False, True])
-def test_more_sequences_than_planner_threads(plan_early):
-    # 1500 one-row spans: the multi-pass planner (the early flag is ignored there)
+@pytest.mark.parametrize("index,block_size", [(1, 16), (2, 16), (3, 16), (4, 16), (5, 16), (3, 8), (5, 128)])
+def test_early_streaming_gives_the_same_rows(index, block_size):
+    # PKV_ATTN_STREAM_EARLY right after the step's kv_append: the decode copies the pages without
+    # a new key while the append may still run; the rows are bit-identical to the plain call's
+    # and match the oracle, over three steps back to back
+    bt = W.config(index, block_size=block_size)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
+                                     bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    outs = []
+    for opts in (None, {"stream_early": True}):
+        d = Dev(bt)
+        for _ in range(3):
+            d.q.copy_(bf16_to_dev(bt.q))
+            d.append()
+            got = ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                                      options=opts)
+        torch.cuda.synchronize()
+        assert ops.get_device_error() == 0
+        outs.append(got)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert_close(outs[1].float().cpu().numpy(), ref, "early streaming")
+
+
+def test_early_streaming_with_rows_of_longer_spans():
+    # no more tokens than sequences but some spans of two or three rows: their rows are decode
+    # entries whose new keys start before their last page, so the decode waits before any page
+    ctx = [40, 33, 17, 64, 5, 100, 16, 31]
+    spans = [2, 0, 1, 3, 0, 1, 0, 1]
+    bt = W.make_batch(ctx, spans, 8, 2, 64, 64, seed=5)
+    assert bt.num_tokens <= bt.num_seqs
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
+                                     bt.rope_theta)
+    ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
+    outs = []
+    for opts in (None, {"stream_early": True}):
+        d = Dev(bt)
+        d.append()
+        outs.append(ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                                        options=opts))
+        torch.cuda.synchronize()
+        assert ops.get_device_error() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert_close(outs[1].float().cpu().numpy(), ref, "early streaming, longer spans")
+
+
+def test_early_streaming_step_in_a_cuda_graph():
+    # the append + attention step captured with PKV_ATTN_STREAM_EARLY replays like eager
+    bt = W.config(3)
+    d = Dev(bt)
+    opts = ops.attention_options({"stream_early": True})
+    out = torch.empty_like(d.q)
+    ws = ops.alloc_workspace(bt.num_tokens, bt.num_seqs, bt.num_q_heads, bt.num_kv_heads, bt.head_dim,
+                             bt.block_tables.shape[1], device=d.q.device)
+    q0 = d.q.clone()
+
+    def step():
+        d.q.copy_(q0)
+        d.append()
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale, out=out,
+                            workspace=ws, options=opts)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    want = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert ops.get_device_error() == 0
+        assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+
+
+@pytest.mark.parametrize("flags", [{}, {"plan_early": True}, {"stream_early": True}])
+def test_more_sequences_than_planner_threads(flags):
+    # 1500 one-row spans: the multi-pass planner (the early flags are ignored there)
     rng = np.random.default_rng(11)
     ctx = rng.integers(1, 200, size=1500)
     pages = int(sum(-(-int(c) // 16) for c in ctx))
@@ -513,7 +593,7 @@ def test_more_sequences_than_planner_threads(plan_early):
     ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
     d = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
     got = ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
-                              options={"plan_early": plan_early})
+                              options=flags)
     torch.cuda.synchronize()
     assert ops.get_device_error() == 0
     assert_close(got.float().cpu().numpy(), ref, "1500 sequences")
