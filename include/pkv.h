@@ -399,10 +399,14 @@ PKV_API int pkv_set_kernel_events(int which, void* start_event, void* stop_event
  * issues no copy and no barrier arrival, so every consumer wait of a CTA with work runs out
  * after about 2^31 SM clocks (about one second), sets PKV_DEVERR_TIMEOUT in the error word
  * and the CTA finishes without further waits; nothing is left in flight and the context
- * stays usable.  The decode rows of such a call are unspecified.  Process-wide.  Returns
- * PKV_ERR_SHAPE for another kind.
+ * stays usable.  The decode rows of such a call are unspecified.
+ * PKV_FAULT_PLAN_NO_READY: with PKV_ATTN_STREAM_EARLY the planner never publishes its ready
+ * word, so every decode CTA's bounded poll of it runs out (2^24 SM clocks, about 8 ms) and the
+ * CTA falls back to waiting for the planner's end: the call is slower but its rows are
+ * correct and no error is reported.  Process-wide.  Returns PKV_ERR_SHAPE for another kind.
  */
 #define PKV_FAULT_DECODE_NO_COPIES 1
+#define PKV_FAULT_PLAN_NO_READY 2
 PKV_API int pkv_set_fault_injection(int kind);
 
 /*

@@ -142,7 +142,7 @@ int pkv_set_overlap(int on) {
 }
 
 int pkv_set_fault_injection(int kind) {
-  if (kind != 0 && kind != PKV_FAULT_DECODE_NO_COPIES) return PKV_ERR_SHAPE;
+  if (kind != 0 && kind != PKV_FAULT_DECODE_NO_COPIES && kind != PKV_FAULT_PLAN_NO_READY) return PKV_ERR_SHAPE;
   g_fault.store(kind);
   return PKV_OK;
 }

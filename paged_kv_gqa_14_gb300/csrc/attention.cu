@@ -344,6 +344,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 // each decode entry's new keys all lie in its last 16-token page (every entry is a span of
 // one token), 2 when some entry is a row of a longer span.  The kernel still waits on the
 // previous kernel before it ends, so work that waits for its end waits for that kernel too.
+// (`stream` 2, a test-only fault: everything as with 1 but the word is never published, so
+// the decode's bounded polls run out and it falls back to waiting for this kernel's end.)
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel_small(const int32_t* __restrict__ qsl,
                                                                   const int32_t* __restrict__ ctxl,
                                                                   int num_seqs, int64_t num_tokens,
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel_small(const int32_t*
   }
   if (stream) {
     __syncthreads();  // every thread's workspace writes are done
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && stream == 1) {
       __threadfence();
       st_release_gpu(plan.header + kPlanReadyWord, long_rows ? 2 : 1);
     }
@@ -683,7 +685,7 @@ cudaError_t launch_paged_attention(const AttnArgs& a, cudaStream_t stream) {
           ? launch_pdl(plan_kernel_small, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
                        static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps, a.decode_ctas,
                        tile_q, a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.plan_early ? 1 : 0,
-                       a.stream_early ? 1 : 0, a.err)
+                       a.stream_early ? (a.fault == PKV_FAULT_PLAN_NO_READY ? 2 : 1) : 0, a.err)
           : launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.qsl, a.context_lens,
                        static_cast<int>(a.num_seqs), a.num_tokens, a.max_blocks << a.bs_log2, pps, a.decode_ctas,
                        tile_q, a.plan, a.max_tiles, sp, rows_in_decode ? 1 : 0, a.err);

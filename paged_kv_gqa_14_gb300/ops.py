@@ -283,9 +283,11 @@ def set_prefill_kernel(kind):
 
 
 def set_fault_injection(kind):
-    """Test only: ``"decode_no_copies"`` makes the decode producer issue nothing, so its
-    consumers' bounded waits run out (``pkv_set_fault_injection``); ``None`` turns it off."""
-    code = {None: 0, "decode_no_copies": 1}[kind]
+    """Test only (``pkv_set_fault_injection``): ``"decode_no_copies"`` makes the decode producer
+    issue nothing, so its consumers' bounded waits run out; ``"plan_no_ready"`` keeps the
+    planner from publishing its ready word under ``stream_early``, so the decode's bounded polls
+    run out and it falls back to the planner's end; ``None`` turns it off."""
+    code = {None: 0, "decode_no_copies": 1, "plan_no_ready": 2}[kind]
     _lib.check("pkv_set_fault_injection", _lib.load().pkv_set_fault_injection(code))
 
 

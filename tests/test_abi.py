@@ -126,6 +126,14 @@ def test_set_overlap(lib):
     assert lib.pkv_set_overlap(1) == 0
 
 
+def test_set_fault_injection(lib):
+    # the two test-only faults and "off"; any other kind is refused
+    for kind in (3, -1, 100):
+        assert lib.pkv_set_fault_injection(kind) == 2  # PKV_ERR_SHAPE
+    for kind in (1, 2, 0):
+        assert lib.pkv_set_fault_injection(kind) == 0
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load(str(tmp_path / "missing.so"))

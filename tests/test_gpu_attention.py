@@ -547,6 +547,49 @@ def test_early_streaming_with_rows_of_longer_spans():
     assert_close(outs[1].float().cpu().numpy(), ref, "early streaming, longer spans")
 
 
+@pytest.mark.parametrize("decode_kernel", ["simt", "tensor"])
+def test_early_streaming_with_either_decode_kernel(decode_kernel):
+    # the CUDA-core decode ignores the ready word and waits for the planner's end; the
+    # tensor-core one streams early: both give the rows of the plain call on the mixed batch
+    bt = W.config(5)
+    outs = []
+    for opts in ({"decode_kernel": decode_kernel}, {"decode_kernel": decode_kernel, "stream_early": True}):
+        d = Dev(bt)
+        d.append()
+        outs.append(ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                                        options=opts))
+        torch.cuda.synchronize()
+        assert ops.get_device_error() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_early_streaming_falls_back_when_the_plan_is_never_published():
+    # the test-only fault keeps the planner from publishing its ready word: every decode CTA's
+    # bounded poll runs out (2^24 SM clocks) and it waits for the planner's end instead, so the
+    # call is slower but its rows are the plain call's, with no device error
+    import time
+
+    bt = W.config(3)
+    q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
+                                     bt.rope_theta)
+    d = Dev(bt, q=q_rot, k_cache=kc, v_cache=vc)
+    want = d.attend().clone()
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    ops.set_fault_injection("plan_no_ready")
+    try:
+        t0 = time.perf_counter()
+        got = ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, d.qsl, bt.scale,
+                                  options={"stream_early": True})
+        torch.cuda.synchronize()
+        waited = time.perf_counter() - t0
+    finally:
+        ops.set_fault_injection(None)
+    assert ops.get_device_error() == 0
+    assert waited > 2e-3  # the polls ran out (about 8 ms at 2 GHz)
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
 def test_early_streaming_step_in_a_cuda_graph():
     # the append + attention step captured with PKV_ATTN_STREAM_EARLY replays like eager
     bt = W.config(3)
