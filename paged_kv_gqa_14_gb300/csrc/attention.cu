@@ -9,7 +9,11 @@
 //      ... and the CTA that writes the last split state of a sequence cut by a CTA boundary
 //      merges that sequence's states (the split merge runs inside the decode kernel)
 // Every kernel is launched with programmatic dependent launch, so each one's launch and
-// prologue overlap the previous kernel's tail.  A batch with prefill spans instead runs
+// prologue overlap the previous kernel's tail.  Right after the step's kv_append a caller may
+// let the planner do its arithmetic while the append runs (PKV_ATTN_PLAN_EARLY) and, further,
+// publish the plan through a ready word at once, so that the tensor-core decode copies the
+// pages holding no new key before the append has finished (PKV_ATTN_STREAM_EARLY).  A batch
+// with prefill spans instead runs
 // the prefill kernel on a second stream, forked after the planner and joined back before
 // the call returns, at the same time as the decode: the planner gives the prefill P of
 // the SMs and spreads the decode units over the rest (SplitArgs in internal.h).

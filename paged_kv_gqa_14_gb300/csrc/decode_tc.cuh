@@ -23,6 +23,11 @@
 // 16-token page is rows 16j..16j+15 of one block when blocks hold 16 or more tokens; with
 // 8-token blocks it is two boxes of 8 rows from two blocks, [row half][kv head][8 rows].
 //
+// The producer requests a unit's block ids before it waits for the unit's stage, and with
+// early streaming it starts on the plan's ready word instead of the planner's end, waiting for
+// the kernel before the planner only before the first page that may hold a new key; the
+// consumers wait for it before they read q.
+//
 // The kernel is instantiated per block size, with it folded in at compile time.  The decode
 // is sensitive to the producer warp's instruction stream (the warp shares a scheduler with
 // two consumer warps and sits on the ring's refill path): on GB300 a form reading the block

@@ -501,17 +501,19 @@ def test_early_planner_gives_the_same_plan(index):
     assert_close(outs[1].float().cpu().numpy(), ref, "early planner")
 
 
-@pytest.mark.parametrize("index,block_size", [(1, 16), (2, 16), (3, 16), (4, 16), (5, 16), (3, 8), (5, 128)])
-def test_early_streaming_gives_the_same_rows(index, block_size):
+@pytest.mark.parametrize("index,block_size,overlap", [(1, 16, None), (2, 16, None), (3, 16, None), (4, 16, None),
+                                                      (5, 16, None), (5, 16, False), (3, 8, None), (5, 128, None)])
+def test_early_streaming_gives_the_same_rows(index, block_size, overlap):
     # PKV_ATTN_STREAM_EARLY right after the step's kv_append: the decode copies the pages without
     # a new key while the append may still run; the rows are bit-identical to the plain call's
-    # and match the oracle, over three steps back to back
+    # and match the oracle, over three steps back to back (in the serial order, overlap False,
+    # the prefill kernel sits between the planner and the decode)
     bt = W.config(index, block_size=block_size)
     q_rot, kc, vc = oracle.kv_append(bt.q, bt.k, bt.v, bt.positions, bt.slot_mapping, bt.k_cache, bt.v_cache,
                                      bt.rope_theta)
     ref = oracle.paged_attention(q_rot, kc, vc, bt.block_tables, bt.context_lens, bt.query_start_loc, bt.scale)
     outs = []
-    for opts in (None, {"stream_early": True}):
+    for opts in ({"overlap": overlap}, {"overlap": overlap, "stream_early": True}):
         d = Dev(bt)
         for _ in range(3):
             d.q.copy_(bf16_to_dev(bt.q))
