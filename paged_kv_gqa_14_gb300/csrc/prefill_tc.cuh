@@ -28,6 +28,11 @@
 //              TMEM, double-buffered, so P of tile f + 1 never waits for P.V of tile f.  O in TMEM is rescaled only when the row max grows by more
 //              than 2^8 (the stale max stays the reference otherwise; O and l share it, so the
 //              result is unchanged).  At the end it reads O, divides by l and stores bf16.
+// A CTA's items follow one another without a CTA barrier: the K and V rings, the S and P
+// buffers and their barrier phases run on across items, the next item's Q tile is loaded once
+// every QK of the current one has completed (q_empty), and its first P.V, which overwrites O,
+// waits until the current item's epilogue has read O (o_free); so the next item's loads, QK and
+// first softmax overlap the current item's last tiles and epilogue.
 // Every wait is bounded; a CTA that times out sets PKV_DEVERR_TIMEOUT and finishes its items
 // without further work.
 #pragma once
@@ -128,6 +133,8 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   uint64_t* fin = bars + 22;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 23);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+  uint64_t* q_empty = bars + 25;  // every QK of an item completed: its Q tile may be replaced
+  uint64_t* o_free = bars + 26;   // the item's epilogue read O: the next item's P.V may write it
   static_assert(C::KST == 3 && C::VST == 3, "barrier layout");
   // P.V of tile t completes pv_done[t % 2] for the (t / 2)-th time
   auto pv_wait = [&](int t) { return warp_wait(&pv_done[t & 1], (t >> 1) & 1, p.err, abort_flag); };
@@ -154,6 +161,8 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
       mbar_init(&pv_done[s], 1);
     }
     mbar_init(fin, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(o_free, 4);
     fence_mbar_init();
     *abort_flag = 0;
   }
@@ -240,7 +249,10 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
 
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer: Q and K
+      // (items follow one another without a CTA barrier: the next item's Q replaces this one
+      // once every QK of this item has completed, and its K tiles follow in the same ring)
       bool ok = !*abort_flag;
+      if (ok && item_no > 0) ok = warp_wait(q_empty, (item_no - 1) & 1, p.err, abort_flag);
       if (ok) {
         if (lane == 0) mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(HALVES * G * PR * 128));
         __syncwarp();
@@ -269,6 +281,8 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
         auto issue_pv = [&](int fp, bool first) -> bool {
           if (!wait_or_abort(vt_full, fp & 1, p.err, abort_flag)) return false;
           if (!wait_or_abort(&p_full[fp & 1], (fp >> 1) & 1, p.err, abort_flag)) return false;
+          // the item's first P.V overwrites O: the previous item's epilogue must have read it
+          if (first && item_no > 0 && !wait_or_abort(o_free, (item_no - 1) & 1, p.err, abort_flag)) return false;
           tc5::fence_after();
           const uint32_t vst = sb + C::OFF_V + (fp % C::VST) * C::kKVBytes;
 #pragma unroll
@@ -295,6 +309,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
           }
           tc5::commit(&s_full[s]);
           tc5::commit(&k_empty[ks]);
+          if (jt == nkt - 1) tc5::commit(q_empty);  // the item's last QK: Q may be replaced
           if (jt > 0) ok = issue_pv(f - 1, jt == 1);
         }
         if (ok) issue_pv(t_glob + nkt - 1, nkt == 1);
@@ -475,12 +490,14 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
           }
         }
         tc5::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);  // O is read: the next item's P.V may overwrite it
       }
     }
     t_glob += nkt;
     ++item_no;
-    __syncthreads();  // the item's buffers (Q, S, O, P) are free for the next item
   }
+  __syncthreads();  // every role has finished its last item (the softmax warps read TMEM to the end)
 
   // teardown: no MMA may still be in flight when TMEM is released
   if (warp == 1) {
